@@ -1,0 +1,314 @@
+// Host core of the invariant_gemm C ABI: argument validation, the plan (a
+// function of K, r, N, slices, split_k, mode and path, never of M), the
+// workspace layout, and the launch sequence of each entry point.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ig_common.cuh"
+
+namespace ig {
+namespace {
+
+struct Plan {
+  int path;          // IG_PATH_FMA / IG_PATH_MMA
+  int mode;
+  int S;             // partitions
+  int64_t Ks;        // K / S
+  int bn;            // shrink rank columns per tile
+  int jblocks;       // r / bn
+  int64_t tiles;     // shrink tiles upper bound (groups 0..L)
+  int64_t etiles;    // expand tiles upper bound (groups 0..L-1)
+  int ntiles;        // expand column tiles per slice
+  size_t off_perm, off_offsets, off_partials, total;
+  uint64_t key;
+};
+
+uint64_t fnv1a(uint64_t h, int64_t v) {
+  for (int i = 0; i < 8; ++i) {
+    h ^= (uint64_t)((v >> (8 * i)) & 0xff);
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+int make_plan(const ig_shape* sh, Plan* pl) {
+  if (!sh || !pl) return IG_ERR_ARG;
+  if (sh->reserved != 0) return IG_ERR_ARG;
+  if (sh->mode < IG_MODE_DET || sh->mode > IG_MODE_UNSPLIT) return IG_ERR_ARG;
+  if (sh->path < IG_PATH_AUTO || sh->path > IG_PATH_MMA) return IG_ERR_ARG;
+  const int64_t M = sh->M, K = sh->K, N = sh->N, r = sh->r;
+  if (M < 0 || K < 8 || N < 8 || r < 8) return IG_ERR_SHAPE;
+  if (K % 8 || N % 8 || r % 8) return IG_ERR_SHAPE;
+  if (sh->slices < 1 || sh->num_adapters < 1) return IG_ERR_SHAPE;
+  const int64_t lim = (int64_t)1 << 40;
+  if (M > (1ll << 31) - 1 || K > lim || N > lim || r > 256) return IG_ERR_UNSUPPORTED;
+  if (M * K > ((int64_t)1 << 46) || (int64_t)sh->slices * N * r > lim) return IG_ERR_UNSUPPORTED;
+  if (sh->num_adapters > kMaxAdapters) return IG_ERR_UNSUPPORTED;
+  int S = sh->mode == IG_MODE_UNSPLIT ? 1 : sh->split_k;
+  if (S < 1) return IG_ERR_SHAPE;
+  if ((K / 8) % S) return IG_ERR_SHAPE;
+  int path = sh->path == IG_PATH_AUTO ? IG_PATH_FMA : sh->path;
+  if (path == IG_PATH_MMA) return IG_ERR_UNSUPPORTED;
+
+  pl->path = path;
+  pl->mode = sh->mode;
+  pl->S = S;
+  pl->Ks = K / S;
+  pl->bn = (r % 16 == 0) ? 16 : 8;
+  pl->jblocks = (int)(r / pl->bn);
+  const int L = sh->num_adapters;
+  pl->tiles = tiles_upper_bound(M, L + 1, kShrinkBM);
+  pl->etiles = tiles_upper_bound(M, L, kExpandBM);
+  pl->ntiles = (int)((N + kExpandBN - 1) / kExpandBN);
+  const int64_t slots = pl->tiles * sh->slices * pl->jblocks;
+  if (sh->mode == IG_MODE_DET && slots > kMaxCounters) return IG_ERR_UNSUPPORTED;
+
+  pl->off_perm = kMapOffset;
+  pl->off_offsets = align_up(pl->off_perm + 4 * (size_t)M, 256);
+  pl->off_partials = align_up(pl->off_offsets + 4 * (size_t)(L + 2), 256);
+  size_t part = 0;
+  if (sh->mode == IG_MODE_DET) part = (size_t)slots * S * kShrinkBM * pl->bn * sizeof(float);
+  pl->total = align_up(pl->off_partials + part, 256);
+
+  uint64_t h = 1469598103934665603ull;
+  const int64_t fields[] = {IG_ABI_VERSION, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
+                            pl->bn, kShrinkKB, kShrinkRowsPerWarp, kExpandJC};
+  for (int64_t f : fields) h = fnv1a(h, f);
+  pl->key = h;
+  return IG_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (!ws) return IG_ERR_ARG;
+  if (!aligned16(ws)) return IG_ERR_ALIGN;
+  if (ws_bytes < pl.total) return IG_ERR_WS_SMALL;
+  return IG_OK;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return IG_OK;
+  return IG_ERR_CUDA;
+}
+
+int run_map(const ig_shape* sh, const Plan& pl, const int32_t* idx, uint8_t* ws,
+            cudaStream_t st) {
+  MapParams mp;
+  mp.idx = idx;
+  mp.perm = reinterpret_cast<int32_t*>(ws + pl.off_perm);
+  mp.offsets = reinterpret_cast<int32_t*>(ws + pl.off_offsets);
+  mp.status = reinterpret_cast<uint32_t*>(ws);
+  mp.M = sh->M;
+  mp.L = sh->num_adapters;
+  return cuda_status(launch_map_tokens(mp, st));
+}
+
+int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A, float scale,
+               float* z, uint8_t* ws, cudaStream_t st) {
+  if (pl.mode == IG_MODE_ATOMIC) {
+    cudaError_t e = cudaMemsetAsync(z, 0, sizeof(float) * sh->slices * sh->M * sh->r, st);
+    if (e != cudaSuccess) return IG_ERR_CUDA;
+  }
+  ShrinkParams p;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.A = static_cast<const __nv_bfloat16*>(A);
+  p.perm = reinterpret_cast<const int32_t*>(ws + pl.off_perm);
+  p.offsets = reinterpret_cast<const int32_t*>(ws + pl.off_offsets);
+  p.z = z;
+  p.partials = reinterpret_cast<float*>(ws + pl.off_partials);
+  p.counters = reinterpret_cast<uint32_t*>(ws + kCountersOffset);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.M = sh->M;
+  p.K = sh->K;
+  p.r = sh->r;
+  p.Ks = pl.Ks;
+  p.slices = sh->slices;
+  p.L = sh->num_adapters;
+  p.S = pl.S;
+  p.jblocks = pl.jblocks;
+  p.scale = scale;
+  return cuda_status(launch_shrink_fma(p, pl.mode, pl.bn, pl.tiles, st));
+}
+
+int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
+               uint8_t* ws, cudaStream_t st) {
+  ExpandParams p;
+  p.z = z;
+  p.B = static_cast<const __nv_bfloat16*>(B);
+  p.perm = reinterpret_cast<const int32_t*>(ws + pl.off_perm);
+  p.offsets = reinterpret_cast<const int32_t*>(ws + pl.off_offsets);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.M = sh->M;
+  p.N = sh->N;
+  p.r = sh->r;
+  p.slices = sh->slices;
+  p.L = sh->num_adapters;
+  p.ntiles = pl.ntiles;
+  return cuda_status(launch_expand_fma(p, pl.etiles, st));
+}
+
+}  // namespace
+}  // namespace ig
+
+using namespace ig;
+
+extern "C" {
+
+const char* ig_version(void) { return "invariant_gemm 0.1 (sm_103a)"; }
+
+const char* ig_status_string(int s) {
+  switch (s) {
+    case IG_OK: return "ok";
+    case IG_ERR_ARG: return "invalid argument (null pointer or enum value)";
+    case IG_ERR_SHAPE: return "invalid shape";
+    case IG_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case IG_ERR_WS_SMALL: return "workspace too small";
+    case IG_ERR_CUDA: return "CUDA runtime error";
+    case IG_ERR_WS_CORRUPT: return "completion counter corrupt";
+    case IG_ERR_ADAPTER_RANGE: return "adapter index out of range";
+    case IG_ERR_TIMEOUT: return "bounded device wait expired";
+    case IG_ERR_UNSUPPORTED: return "unsupported by this build";
+    default: return "unknown status";
+  }
+}
+
+size_t ig_workspace_bytes(const ig_shape* shape) {
+  Plan pl;
+  if (make_plan(shape, &pl) != IG_OK) return 0;
+  return pl.total;
+}
+
+int ig_plan_query(const ig_shape* shape, ig_plan_info* out) {
+  if (!out) return IG_ERR_ARG;
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  memset(out, 0, sizeof(*out));
+  out->path = pl.path;
+  out->split_k = pl.S;
+  out->k_split = pl.Ks;
+  out->shrink_bm = kShrinkBM;
+  out->shrink_bn = pl.bn;
+  out->expand_bm = kExpandBM;
+  out->expand_bn = kExpandBN;
+  out->shrink_tiles_max = pl.tiles;
+  out->shrink_ctas_max = pl.tiles * shape->slices * pl.jblocks * pl.S;
+  out->workspace_bytes = (int64_t)pl.total;
+  out->determinism_key = pl.key;
+  return IG_OK;
+}
+
+int ig_workspace_init(void* ws, size_t ws_bytes, const ig_shape* shape, void* stream) {
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  rc = check_ws(pl, ws, ws_bytes);
+  if (rc != IG_OK) return rc;
+  cudaError_t e = cudaMemsetAsync(ws, 0, kMapOffset, static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+int ig_map_tokens(const ig_shape* shape, const int32_t* adapter_idx, void* ws, size_t ws_bytes,
+                  void* stream) {
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  if (shape->M == 0) return IG_OK;
+  rc = check_ws(pl, ws, ws_bytes);
+  if (rc != IG_OK) return rc;
+  if (!adapter_idx) return IG_ERR_ARG;
+  if (!aligned16(adapter_idx)) return IG_ERR_ALIGN;
+  return run_map(shape, pl, adapter_idx, static_cast<uint8_t*>(ws),
+                 static_cast<cudaStream_t>(stream));
+}
+
+int lora_shrink(const ig_shape* shape, const void* x, const void* A_stack,
+                const int32_t* adapter_idx, float scale, float* z, void* ws, size_t ws_bytes,
+                void* stream) {
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  if (shape->M == 0) return IG_OK;
+  rc = check_ws(pl, ws, ws_bytes);
+  if (rc != IG_OK) return rc;
+  if (!x || !A_stack || !z) return IG_ERR_ARG;
+  if (!aligned16(x) || !aligned16(A_stack) || !aligned16(z) ||
+      (adapter_idx && !aligned16(adapter_idx)))
+    return IG_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (adapter_idx) {
+    rc = run_map(shape, pl, adapter_idx, w, st);
+    if (rc != IG_OK) return rc;
+  }
+  return run_shrink(shape, pl, x, A_stack, scale, z, w, st);
+}
+
+int lora_expand(const ig_shape* shape, const float* z, const void* B_stack,
+                const int32_t* adapter_idx, void* y, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  if (shape->M == 0) return IG_OK;
+  rc = check_ws(pl, ws, ws_bytes);
+  if (rc != IG_OK) return rc;
+  if (!z || !B_stack || !y) return IG_ERR_ARG;
+  if (!aligned16(z) || !aligned16(B_stack) || !aligned16(y) ||
+      (adapter_idx && !aligned16(adapter_idx)))
+    return IG_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (adapter_idx) {
+    rc = run_map(shape, pl, adapter_idx, w, st);
+    if (rc != IG_OK) return rc;
+  }
+  return run_expand(shape, pl, z, B_stack, y, w, st);
+}
+
+int lora_apply(const ig_shape* shape, const void* x, void* y, const int32_t* adapter_idx,
+               const void* A_stack, const void* B_stack, float scale, float* z, void* ws,
+               size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  if (shape->M == 0) return IG_OK;
+  rc = check_ws(pl, ws, ws_bytes);
+  if (rc != IG_OK) return rc;
+  if (!x || !y || !A_stack || !B_stack || !z) return IG_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(A_stack) || !aligned16(B_stack) ||
+      !aligned16(z) || (adapter_idx && !aligned16(adapter_idx)))
+    return IG_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (adapter_idx) {
+    rc = run_map(shape, pl, adapter_idx, w, st);
+    if (rc != IG_OK) return rc;
+  }
+  rc = run_shrink(shape, pl, x, A_stack, scale, z, w, st);
+  if (rc != IG_OK) return rc;
+  return run_expand(shape, pl, z, B_stack, y, w, st);
+}
+
+int ig_check_status(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return IG_ERR_ARG;
+  if (ws_bytes < kMapOffset) return IG_ERR_WS_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return IG_ERR_CUDA;
+  uint32_t status = 0;
+  if (cudaMemcpy(&status, ws, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return IG_ERR_CUDA;
+  if (status == 0) return IG_OK;
+  // Clear the word; after a corrupt counter or an abandoned tile, zero the
+  // counters too so that the workspace is usable again.
+  size_t clear = (status & (kStatusCorrupt | kStatusTimeout)) ? kMapOffset : sizeof(uint32_t);
+  if (cudaMemsetAsync(ws, 0, clear, st) != cudaSuccess) return IG_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return IG_ERR_CUDA;
+  if (status & kStatusTimeout) return IG_ERR_TIMEOUT;
+  if (status & kStatusCorrupt) return IG_ERR_WS_CORRUPT;
+  return IG_ERR_ADAPTER_RANGE;
+}
+
+}  // extern "C"

@@ -1,0 +1,219 @@
+// Internal definitions shared by the kernels and the host core of the
+// invariant_gemm library: workspace layout, device status bits, launch
+// parameter blocks, and small device helpers (bf16 conversion, mbarrier and
+// bulk-copy wrappers, bounded waits).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/invariant_gemm.h"
+
+namespace ig {
+
+// ---------------------------------------------------------------------------
+// workspace layout
+//
+//   [0, 256)                      status words (u32 status at offset 0)
+//   [256, 256 + 4*kMaxCounters)   per-tile completion counters (u32)
+//   [kMapOffset, ...)             token map: perm[M] int32, then
+//                                 offsets[G+1] int32 at a 256-byte boundary
+//   [partials, ...)               FP32 partials [slots][S][BM*BN] (DET only)
+//
+// The counters sit at a fixed place whatever the shape, so one
+// ig_workspace_init makes a workspace valid for every later call that fits
+// in it: counters are only ever left at zero (Algorithm 1, line 14).
+// ---------------------------------------------------------------------------
+constexpr int64_t kMaxCounters = 65536;
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kCountersOffset = kStatusBytes;
+constexpr size_t kMapOffset = kCountersOffset + 4 * kMaxCounters;
+constexpr int kMaxAdapters = 1023;  // token-map groups G = L + 1 <= 1024
+
+constexpr uint32_t kStatusAdapterRange = 1u << 0;
+constexpr uint32_t kStatusCorrupt = 1u << 1;
+constexpr uint32_t kStatusTimeout = 1u << 2;
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a) {
+  return (v + a - 1) / a * a;
+}
+
+// FMA-path tile geometry (fixed: part of the determinism key).
+constexpr int kShrinkWarps = 8;
+constexpr int kShrinkRowsPerWarp = 4;
+constexpr int kShrinkBM = kShrinkWarps * kShrinkRowsPerWarp;  // 32 token rows
+constexpr int kShrinkKB = 256;        // elements per k-block: 32 lanes x 8
+constexpr int kShrinkStages = 4;
+constexpr int kExpandWarps = 8;
+constexpr int kExpandRowsPerWarp = 4;
+constexpr int kExpandBM = kExpandWarps * kExpandRowsPerWarp;  // 32 token rows
+constexpr int kExpandBN = 256;        // output columns: 32 lanes x 8
+constexpr int kExpandJC = 8;          // rank elements per register chunk
+
+// Tile count over token groups: sum over groups g of ceil(count_g / bm),
+// bounded by floor(M / bm) + (number of non-empty groups).
+inline int64_t tiles_upper_bound(int64_t M, int64_t groups, int64_t bm) {
+  if (M <= 0) return 0;
+  int64_t ne = groups < M ? groups : M;
+  return M / bm + ne;
+}
+
+struct MapParams {
+  const int32_t* idx;
+  int32_t* perm;
+  int32_t* offsets;
+  uint32_t* status;
+  int64_t M;
+  int32_t L;
+};
+
+struct ShrinkParams {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* A;
+  const int32_t* perm;
+  const int32_t* offsets;
+  float* z;
+  float* partials;
+  uint32_t* counters;
+  uint32_t* status;
+  int64_t M, K, r, Ks;
+  int32_t slices, L, S, jblocks;
+  float scale;
+};
+
+struct ExpandParams {
+  const float* z;
+  const __nv_bfloat16* B;
+  const int32_t* perm;
+  const int32_t* offsets;
+  __nv_bfloat16* y;
+  uint32_t* status;
+  int64_t M, N, r;
+  int32_t slices, L, ntiles;
+};
+
+// Launchers (defined in the .cu files); they return cudaGetLastError().
+cudaError_t launch_map_tokens(const MapParams& p, cudaStream_t st);
+cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn,
+                              int64_t tiles_max, cudaStream_t st);
+cudaError_t launch_expand_fma(const ExpandParams& p, int64_t tiles_max,
+                              cudaStream_t st);
+
+#ifdef __CUDACC__
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
+  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+
+// FP32 -> BF16, round to nearest, ties to even (cvt.rn.bf16.f32).
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return (uint32_t)__bfloat16_as_ushort(h);
+}
+__device__ __forceinline__ float bf16_round_f32(float f) {
+  return __uint_as_float(f32_to_bf16_bits(f) << 16);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase. Gives up after ~2^31 SM clocks (about a
+// second), records kStatusTimeout and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > (1ll << 31)) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// One-dimensional bulk copy global -> shared, completion counted in bytes on
+// the mbarrier. dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Locate output tile `t` among token groups [0, G): group g holds rows
+// offsets[g] .. offsets[g+1]-1 of the permuted order and ceil(count/bm)
+// tiles. Called by one full warp; every lane gets the result. Returns false
+// when t is past the last tile.
+__device__ __forceinline__ bool find_tile(const int32_t* offsets, int G, int bm, int64_t t,
+                                          int* g_out, int* row0_out, int* nrows_out) {
+  const int lane = threadIdx.x & 31;
+  int64_t before = 0;
+  for (int base = 0; base < G; base += 32) {
+    const int g = base + lane;
+    int cnt = 0;
+    if (g < G) cnt = offsets[g + 1] - offsets[g];
+    int64_t tl = (cnt + bm - 1) / bm;
+    int64_t incl = tl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+    if (t < before + total) {
+      const unsigned hit = __ballot_sync(0xffffffffu, t < before + incl);
+      const int src = __ffs(hit) - 1;
+      const int64_t excl = __shfl_sync(0xffffffffu, incl - tl, src);
+      const int c = __shfl_sync(0xffffffffu, cnt, src);
+      const int q = (int)(t - before - excl);
+      *g_out = base + src;
+      *row0_out = q * bm;
+      *nrows_out = min(bm, c - q * bm);
+      return true;
+    }
+    before += total;
+  }
+  return false;
+}
+#endif  // __CUDACC__
+
+}  // namespace ig

@@ -1,0 +1,147 @@
+"""CUDA path against the FP64 oracle, element by element, through the C ABI.
+
+Shapes follow the workloads of "Reproducible LoRA Inference Through
+Deterministic Split-K Reduction" (decode and prefill, ranks 16-128, fused QKV
+slices, Split-K 8) and cover several tiles, ragged tails (rows, K partitions
+that are not whole k-blocks, output columns), tokens without an adapter, and
+the largest sizes on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import invariant_gemm_gb300 as ig
+import synth
+from helpers import (bits, check_expand, check_shrink, need_gpu, run_apply, shape_of)
+
+pytestmark = pytest.mark.gpu
+
+MODES = [ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT]
+MODE_ID = {ig.MODE_DET: "det", ig.MODE_ATOMIC: "atomic", ig.MODE_UNSPLIT: "unsplit"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def cpu(prob):
+    return prob.to("cpu")
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_single_adapter_small_normal(mode):
+    p = synth.make_problem(4, 512, 512, 8, L=1, seed=1000, device="cuda")
+    z, y = run_apply(p, mode=mode)
+    check_shrink(cpu(p), z)
+    check_expand(cpu(p), z, y)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_single_adapter_small_integers_bit_exact(mode):
+    p = synth.make_problem(4, 512, 512, 8, L=1, seed=1000, dist="int", device="cuda")
+    z, y = run_apply(p, mode=mode)
+    check_shrink(cpu(p), z, exact=True)
+    check_expand(cpu(p), z, y, exact=True)
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 128, 256])
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_decode_7b(M, mode):
+    p = synth.make_problem(M, 4096, 4096, 16, L=8, seed=1001 + M, device="cuda")
+    z, y = run_apply(p, mode=mode)
+    check_shrink(cpu(p), z)
+    check_expand(cpu(p), z, y)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_decode_7b_integers_bit_exact(mode):
+    # |sum| <= 4096 * 16 < 2^24 and every expand sum < 2^24: all orders exact
+    p = synth.make_problem(256, 4096, 4096, 16, L=8, seed=77, dist="int", device="cuda")
+    z, y = run_apply(p, mode=mode)
+    check_shrink(cpu(p), z, exact=True)
+    check_expand(cpu(p), z, y, exact=True)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_ragged_everything(mode):
+    # K/S = 1376 (5 whole k-blocks + 96), r = 24 (three 8-column blocks),
+    # N = 264 (a partial column tile), 3 slices, 5 adapters, 20% no-adapter rows
+    p = synth.make_problem(300, 11008, 264, 24, slices=3, L=5, seed=5, none_frac=0.2,
+                           device="cuda")
+    z, y = run_apply(p, mode=mode)
+    check_shrink(cpu(p), z)
+    check_expand(cpu(p), z, y)
+    zc = z.cpu().numpy()
+    none = p.idx.cpu().numpy() < 0
+    assert none.any() and np.all(zc[:, none] == 0)
+
+
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16, 64])
+def test_split_counts(S):
+    p = synth.make_problem(40, 4096, 512, 16, L=3, seed=60 + S, device="cuda")
+    z, y = run_apply(p, mode=ig.MODE_DET, split_k=S)
+    check_shrink(cpu(p), z)
+    check_expand(cpu(p), z, y)
+
+
+def _sample_rows(M, n, seed):
+    g = np.random.default_rng(seed)
+    rows = set(g.choice(M, size=min(M, n), replace=False).tolist())
+    rows.update({0, M - 1})
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("which", ["qkv", "down"])
+@pytest.mark.parametrize("mode", [ig.MODE_DET, ig.MODE_UNSPLIT], ids=MODE_ID.get)
+def test_prefill_sampled_rows(which, mode):
+    if which == "qkv":
+        p = synth.make_problem(4096, 4096, 4096, 64, slices=3, L=16, ids="segments",
+                               segment=256, seed=1002, device="cuda")
+    else:
+        p = synth.make_problem(4096, 11008, 4096, 64, slices=1, L=16, ids="segments",
+                               segment=256, seed=1012, device="cuda")
+    z, y = run_apply(p, mode=mode)
+    rows = _sample_rows(p.M, 48, 3)
+    rows = np.union1d(rows, [255, 256, 257, 4095])
+    check_shrink(cpu(p), z, rows=rows)
+    check_expand(cpu(p), z, y, rows=rows)
+
+
+LARGE = [(8192, 1, 8), (8192, 256, 8), (8192, 2048, 4), (28672, 16, 16), (28672, 8192, 16),
+         (28672, 256, 1)]
+
+
+@pytest.mark.parametrize("K,M,S", LARGE)
+@pytest.mark.parametrize("mode", [ig.MODE_DET, ig.MODE_ATOMIC], ids=MODE_ID.get)
+def test_large_model_sampled_rows(K, M, S, mode):
+    if S == 1 and mode == ig.MODE_ATOMIC:
+        pytest.skip("Split-K = 1 has nothing to add atomically")
+    p = synth.make_problem(M, K, 8192, 128, L=64, ids="zipf", seed=1004, device="cuda")
+    z, y = run_apply(p, mode=mode, split_k=S)
+    rows = _sample_rows(M, 24, K + M)
+    # the oracle only needs the sampled rows; keep the host copies small
+    sub = synth.Problem(M=len(rows), K=K, N=p.N, r=p.r, slices=1, L=p.L, scale=p.scale,
+                        x=p.x[torch.as_tensor(rows, device="cuda")].cpu(), A=p.A.cpu(),
+                        B=p.B.cpu(), y=p.y[torch.as_tensor(rows, device="cuda")].cpu(),
+                        idx=p.idx[torch.as_tensor(rows, device="cuda")].cpu())
+    rt = torch.as_tensor(rows, device="cuda")
+    check_shrink(sub, z[:, rt])
+    check_expand(sub, z[:, rt], y[rt])
+
+
+def test_zero_tokens():
+    p = synth.make_problem(0, 512, 512, 8, L=1, seed=1, device="cuda")
+    z, y = run_apply(p)
+    assert z.numel() == 0 and y.numel() == 0
+
+
+def test_max_adapters_and_all_none():
+    p = synth.make_problem(700, 512, 256, 16, L=1023, seed=8, device="cuda")
+    z, y = run_apply(p)
+    check_shrink(cpu(p), z)
+    check_expand(cpu(p), z, y)
+    p.idx.fill_(-1)
+    z, y = run_apply(p)
+    assert torch.all(z == 0)
+    assert torch.equal(y, p.y)
