@@ -205,9 +205,11 @@ def test_token_map_reuse_across_layers():
 
 
 def test_workspace_reused_across_shapes_without_reinit():
-    big = ig.make_shape(512, 4096, 1024, 32, num_adapters=8, split_k=8)
-    ws = ig.workspace(big)
-    for M, S, r in [(512, 8, 32), (7, 4, 16), (300, 16, 32), (1, 8, 16), (512, 8, 32)]:
+    cases = [(512, 8, 32), (7, 4, 16), (300, 16, 32), (1, 8, 16), (512, 8, 32)]
+    need = max(ig.workspace_bytes(ig.make_shape(M, 4096, 1024, r, num_adapters=8, split_k=S))
+               for M, S, r in cases)
+    ws = ig.workspace(ig.make_shape(1, 4096, 1024, 16, num_adapters=8), min_bytes=need)
+    for M, S, r in cases:
         p = synth.make_problem(M, 4096, 1024, r, L=8, seed=M * 10 + S, device="cuda")
         z, y = run_apply(p, mode=ig.MODE_DET, split_k=S, ws=ws)
         check_shrink(p.to("cpu"), z)
