@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Throughput of the multi-adapter LoRA shrink+expand path on one GB300.
+
+Workload (decode, 7B-like dimensions): M = 256 tokens, K = 4096, r = 16,
+N = 4096, 8 adapters with a uniform per-token adapter index, Split-K = 8,
+bf16 in, FP32 shrink output, bf16 expand into y. One step is one decode step
+through a stack of 64 LoRA-adapted linear layers, each with its own x, y,
+A_stack and B_stack (384 MB in all, larger than the 129 MB L2, so no layer
+finds its inputs in L2): the token map is built once per step and shared by
+the 64 lora_apply calls (map -> shrink -> expand per layer). The step is
+captured in a CUDA graph and replayed.
+
+value: token rows through one shrink+expand per second, i.e.
+M * layers / step time, deterministic Split-K = 8, inputs resident in HBM.
+Also reported: the atomic Split-K = 8 and unsplit variants, a sweep over
+M in {1, 8, 32, 128, 256}, HBM GB/s of the algorithmic bytes, the dominant
+kernel's roofline, the end-to-end number with host buffers, and the FP64
+oracle timed on the host cores.
+
+`--impl reference` times the FP64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import os
+
+# the oracle's numpy/BLAS use one thread, so the CPU baseline's core count is exact
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+WORKLOAD = dict(M=256, K=4096, N=4096, r=16, slices=1, L=8, S=8, layers=64, scale=2.0)
+SWEEP_M = [1, 8, 32, 128, 256]
+METRIC = "LoRA shrink+expand tokens/s, HBM GB/s % roofline (det Split-K vs atomic, unsplit)"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value over all ranks (timing only, not on the data path)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def alg_bytes(M, K, N, r, slices, u):
+    """Bytes the method must move (shrink and expand), per lora_apply."""
+    shrink = 2 * M * K + u * 2 * K * r * slices + 4 * M * r * slices + 4 * M
+    expand = 4 * M * r * slices + u * 2 * N * r * slices + 4 * M * N * slices + 4 * M
+    return {"shrink": shrink, "expand": expand, "total": shrink + expand}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+class Stack:
+    """`layers` LoRA layers sharing one batch of adapter indices."""
+
+    def __init__(self, M, K, N, r, slices, L, layers, scale, seed, device):
+        import synth
+        g = torch.Generator(device=device).manual_seed(seed)
+        self.M, self.K, self.N, self.r, self.slices, self.L = M, K, N, r, slices, L
+        self.layers, self.scale = layers, scale
+        self.idx = synth.adapter_ids(M, L, "uniform", g, device)
+        self.x, self.y0, self.A, self.B = [], [], [], []
+        for l in range(layers):
+            p = synth.make_problem(M, K, N, r, slices=slices, L=L, scale=scale,
+                                   seed=seed * 1000 + l, device=device)
+            self.x.append(p.x)
+            self.y0.append(p.y)
+            self.A.append(p.A)
+            self.B.append(p.B)
+        self.y = [t.clone() for t in self.y0]
+        self.z = torch.empty((slices, M, r), dtype=torch.float32, device=device)
+        self.u = int(torch.unique(self.idx[self.idx >= 0]).numel())
+
+    def bytes_resident(self):
+        n = 0
+        for ts in (self.x, self.y, self.A, self.B):
+            n += sum(t.numel() * t.element_size() for t in ts)
+        return n
+
+
+def make_shape(ig, st: Stack, mode, M=None):
+    return ig.make_shape(st.M if M is None else M, st.K, st.N, st.r, slices=st.slices,
+                         num_adapters=st.L, split_k=WORKLOAD["S"], mode=mode)
+
+
+def run_step(ig, st: Stack, sh, ws, M=None, stream=None):
+    """One step: token map once, then every layer's shrink+expand. Returns the
+    number of kernels of this library it launched."""
+    M = st.M if M is None else M
+    idx = st.idx[:M]
+    ig.map_tokens(sh, idx, ws, stream)
+    for l in range(st.layers):
+        ig.lora_apply(sh, st.x[l][:M], st.y[l][:M], None, st.A[l], st.B[l], st.scale,
+                      st.z[:, :M] if M == st.M else st.z_small[M], ws, stream)
+    return 1 + 2 * st.layers
+
+
+def capture(ig, st, sh, ws, M=None):
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(2):                       # warm the launch path before capture
+            run_step(ig, st, sh, ws, M, stream)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        n = run_step(ig, st, sh, ws, M, torch.cuda.current_stream())
+    return g, n
+
+
+def time_graph(g, steps, warmup, world, device):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, world, device)
+
+
+def kernel_durations(ig, st, sh, ws, reps=3):
+    """Average device duration of one shrink launch and one expand launch,
+    CUDA events around each launch on the launching stream."""
+    stream = torch.cuda.current_stream()
+    ig.map_tokens(sh, st.idx, ws)
+    ev = []
+    for _ in range(reps):
+        for l in range(st.layers):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            ig.lora_shrink(sh, st.x[l], st.A[l], None, st.scale, st.z, ws)
+            e[1].record(stream)
+            ig.lora_expand(sh, st.z, st.B[l], None, st.y[l], ws)
+            e[2].record(stream)
+            ev.append(e)
+    torch.cuda.synchronize()
+    sh_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ex_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    return sh_ms, ex_ms
+
+
+def source_hash(name):
+    path = os.path.join(ROOT, "invariant_gemm_gb300", "csrc", name)
+    try:
+        with open(path, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def ncu_traffic(kernel_file, workload_key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel and on this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_file]
+        if e.get("source_sha256_16") != source_hash(kernel_file):
+            return None
+        if e.get("workload") != workload_key:
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+
+def oracle_sample(seconds: float, seed=7):
+    """Time the FP64 oracle (shrink + expand, as it stands) on a bounded sample
+    of the workload: layers of the same shape, host inputs, until `seconds`
+    of CPU work. Returns (tokens/s, layers done, threads)."""
+    import oracle
+    import synth
+    W = WORKLOAD
+    prob = synth.make_problem(W["M"], W["K"], W["N"], W["r"], slices=W["slices"], L=W["L"],
+                              scale=W["scale"], seed=seed, device="cpu")
+
+    def b(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    x, A, B, y, idx = b(prob.x), b(prob.A), b(prob.B), b(prob.y), prob.idx.numpy()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.apply(x, y, idx, A, B, W["scale"])
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+    return W["M"] * done / dt, done, threads
+
+
+def cpu_baseline_obj(seconds):
+    v, done, threads = oracle_sample(seconds)
+    return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} layers of the workload (M={WORKLOAD['M']}, K={WORKLOAD['K']}, "
+                      f"N={WORKLOAD['N']}, r={WORKLOAD['r']}, 8 adapters) through the FP64 "
+                      f"numpy oracle, shrink+expand, ~{seconds:.0f} s of one core"}
+
+
+def workload_config():
+    W = WORKLOAD
+    return {"workload": (f"decode 7B-like LoRA layer stack: M={W['M']} tokens, K={W['K']}, "
+                         f"r={W['r']}, N={W['N']}, {W['L']} adapters (uniform per-token "
+                         f"index), Split-K={W['S']}, {W['layers']} layers per step"),
+            "M": W["M"], "K": W["K"], "N": W["N"], "r": W["r"], "slices": W["slices"],
+            "adapters": W["L"], "split_k": W["S"], "layers_per_step": W["layers"],
+            "value_counts": "token rows through one shrink+expand (M x layers per step)",
+            "l2": "inputs larger than L2 (distinct tensors per layer, 384 MB per step)"}
+
+
+def reference_main(args, rank, world):
+    if rank != 0:
+        return 0
+    steps, warm = args.steps, args.warmup
+    import oracle  # noqa: F401
+    per = max(0.05, min(20.0, 150.0 / max(1, steps + warm)))
+    for _ in range(warm):
+        oracle_sample(per)
+    vals = []
+    layers = 0
+    for _ in range(steps):
+        v, done, threads = oracle_sample(per)
+        vals.append(v)
+        layers += done
+    value = statistics.mean(vals)
+    ms = WORKLOAD["M"] * WORKLOAD["layers"] / value * 1e3
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": workload_config(),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": f"{layers} layers in {steps} steps of ~{per:.0f} s"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-sweep", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        return reference_main(args, rank, world)
+
+    import invariant_gemm_gb300 as ig
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    W = WORKLOAD
+
+    st = Stack(W["M"], W["K"], W["N"], W["r"], W["slices"], W["L"], W["layers"], W["scale"],
+               seed=1001 + rank, device=device)
+    st.z_small = {m: torch.empty((W["slices"], m, W["r"]), dtype=torch.float32, device=device)
+                  for m in SWEEP_M}
+    ws = {}
+    for mode in (ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT):
+        ws[mode] = ig.workspace(make_shape(ig, st, mode), device=device)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+
+    # main number: deterministic Split-K = 8
+    results = {}
+    graphs = {}
+    for mode, name in ((ig.MODE_DET, "det_sk8"), (ig.MODE_ATOMIC, "atomic_sk8"),
+                       (ig.MODE_UNSPLIT, "unsplit_sk1")):
+        sh = make_shape(ig, st, mode)
+        g, launches = capture(ig, st, sh, ws[mode])
+        graphs[mode] = (g, launches)
+        ms = time_graph(g, args.steps, max(3, args.warmup), world, device)
+        tok = W["M"] * W["layers"] * world / (ms * 1e-3)
+        b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
+        gbs = b["total"] * W["layers"] / (ms * 1e-3) / 1e9
+        results[name] = {"ms_per_step": ms, "tokens_per_s": tok, "hbm_gbs": gbs,
+                         "us_per_layer": ms * 1e3 / W["layers"]}
+    clk = clocks.stop()
+    assert ig.check_status(ws[ig.MODE_DET]) == 0
+
+    peak, peak_kind = measured_peaks()
+    for v in results.values():
+        v["hbm_frac_of_" + peak_kind] = v["hbm_gbs"] / peak
+        v["hbm_frac_of_8tbs_nominal"] = v["hbm_gbs"] / 8000.0
+    det = results["det_sk8"]
+    results["det_overhead_vs_atomic_pct"] = 100 * (det["ms_per_step"] /
+                                                   results["atomic_sk8"]["ms_per_step"] - 1)
+    results["det_speedup_vs_unsplit_pct"] = 100 * (results["unsplit_sk1"]["ms_per_step"] /
+                                                   det["ms_per_step"] - 1)
+
+    # sweep over the decode batch sizes
+    sweep = {}
+    if not args.no_sweep:
+        for M in SWEEP_M:
+            row = {}
+            for mode, name in ((ig.MODE_DET, "det"), (ig.MODE_ATOMIC, "atomic"),
+                               (ig.MODE_UNSPLIT, "unsplit")):
+                sh = make_shape(ig, st, mode, M=M)
+                g, _ = capture(ig, st, sh, ws[mode], M=M)
+                ms = time_graph(g, max(20, args.steps // 4), 3, world, device)
+                u = int(torch.unique(st.idx[:M]).numel())
+                b = alg_bytes(M, W["K"], W["N"], W["r"], W["slices"], u)
+                row[name] = {"us_per_layer": ms * 1e3 / W["layers"],
+                             "tokens_per_s": M * W["layers"] * world / (ms * 1e-3),
+                             "hbm_gbs": b["total"] * W["layers"] / (ms * 1e-3) / 1e9}
+                del g
+            sweep[str(M)] = row
+
+    # dominant kernel roofline: per-launch CUDA-event durations
+    sh = make_shape(ig, st, ig.MODE_DET)
+    sh_ms, ex_ms = kernel_durations(ig, st, sh, ws[ig.MODE_DET])
+    b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
+    kern = {"shrink_fma (lora_shrink, det)": (sh_ms, b["shrink"], "shrink_fma.cu"),
+            "expand_fma (lora_expand)": (ex_ms, b["expand"], "expand_fma.cu")}
+    dom = max(kern, key=lambda k: kern[k][0])
+    d_ms, d_bytes, d_file = kern[dom]
+    achieved = d_bytes / (d_ms * 1e-3) / 1e9
+    wkey = f"M={W['M']},K={W['K']},N={W['N']},r={W['r']},L={W['L']},S={W['S']}"
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": ncu_traffic(d_file, wkey),
+                "alg_bytes_per_launch": d_bytes, "us_per_launch": d_ms * 1e3,
+                "kernels_us_per_launch": {k: v[0] * 1e3 for k, v in kern.items()}}
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    g, launches = graphs[ig.MODE_DET]
+    hx = [t.cpu().pin_memory() for t in st.x]
+    hy = [t.cpu().pin_memory() for t in st.y0]
+    hidx = st.idx.cpu().pin_memory()
+    hout = [torch.empty_like(t) for t in hy]
+    hout = [t.pin_memory() for t in hout]
+    h2d = sum(t.numel() * t.element_size() for t in hx + hy) + hidx.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    e2e_steps = max(5, min(args.steps, 50))
+
+    def e2e_step():
+        for l in range(W["layers"]):
+            st.x[l].copy_(hx[l], non_blocking=True)
+            st.y[l].copy_(hy[l], non_blocking=True)
+        st.idx.copy_(hidx, non_blocking=True)
+        g.replay()
+        for l in range(W["layers"]):
+            hout[l].copy_(st.y[l], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, world, device)
+    e2e = {"value": W["M"] * W["layers"] * world / (e2e_ms * 1e-3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "how": "pinned host x, y, idx -> device; captured step (C-ABI calls) -> y back"}
+
+    out = {"metric": METRIC, "value": det["tokens_per_s"], "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": det["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic", "config": workload_config(), "clocks": clk,
+           "gpu_launches": launches * args.steps,
+           "roofline": roofline, "variants": results, "sweep_M": sweep, "e2e": e2e,
+           "hbm_gbs": det["hbm_gbs"]}
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline_obj(args.cpu_seconds)
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
