@@ -179,6 +179,32 @@ int lora_apply(const ig_shape* shape, const void* x, void* y,
                const void* B_stack, float scale, float* z,
                void* ws, size_t ws_bytes, void* stream);
 
+/* lora_shrink without a caller-provided workspace. The paper has no
+ * counterpart: it exists for callers that cannot allocate device memory
+ * where they run the shrink (code that must not risk the device-wide
+ * synchronisation an allocation can bring, runtimes that plan all memory
+ * ahead and give libraries no allocator, plugin hosts that own every
+ * allocation).
+ *
+ * Same arguments, arithmetic and results as lora_shrink (adapter_idx must be
+ * non-NULL), but the token map, counters, status word and partials live in
+ * a 4 MiB array inside the library, held by every GPU that loads it until
+ * the process exits. This call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *   - Shapes whose ig_workspace_bytes exceeds 4 MiB are rejected with
+ *     IG_ERR_WS_SMALL before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current). Make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the previous call's
+ *     contents; each call clears the status word and the counters it uses
+ *     (a memset on `stream`). Calls that overlap on the GPU (other streams,
+ *     other threads) race on the array and give wrong results: serialise
+ *     them.
+ *   - Device-side status (out-of-range adapter index, expired wait) is not
+ *     reported; validate adapter_idx beforehand. */
+int lora_shrink_noalloc(const ig_shape* shape, const void* x, const void* A_stack,
+                        const int32_t* adapter_idx, float scale, float* z, void* stream);
+
 /* Synchronise `stream`, read and clear the workspace status word, and return
  * the most severe device-side error recorded since the last check
  * (IG_ERR_TIMEOUT, IG_ERR_WS_CORRUPT, IG_ERR_ADAPTER_RANGE) or IG_OK. After

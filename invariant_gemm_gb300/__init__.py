@@ -22,7 +22,8 @@ __all__ = [
     "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "PATH_AUTO", "PATH_FMA", "PATH_MMA",
     "IGError", "Shape", "PlanInfo", "lib", "lib_path", "make_shape", "workspace_bytes",
     "plan_query", "workspace", "workspace_init", "map_tokens", "lora_shrink",
-    "lora_expand", "lora_apply", "check_status", "status_string", "EXPORTS",
+    "lora_expand", "lora_apply", "lora_shrink_noalloc", "check_status", "status_string",
+    "EXPORTS",
 ]
 
 MODE_DET, MODE_ATOMIC, MODE_UNSPLIT = 0, 1, 2
@@ -38,7 +39,7 @@ STATUS = {
 EXPORTS = [
     "ig_version", "ig_status_string", "ig_workspace_bytes", "ig_plan_query",
     "ig_workspace_init", "ig_map_tokens", "lora_shrink", "lora_expand", "lora_apply",
-    "ig_check_status",
+    "ig_check_status", "lora_shrink_noalloc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
         L.lora_apply.restype = ctypes.c_int
         L.lora_apply.argtypes = [_SP, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P,
                                  ctypes.c_size_t, _P]
+        L.lora_shrink_noalloc.restype = ctypes.c_int
+        L.lora_shrink_noalloc.argtypes = [_SP, _P, _P, _P, ctypes.c_float, _P, _P]
         L.ig_check_status.restype = ctypes.c_int
         L.ig_check_status.argtypes = [_P, ctypes.c_size_t, _P]
         _LIB = L
@@ -198,6 +201,14 @@ def lora_apply(shape: Shape, x, y, adapter_idx, A_stack, B_stack, scale, z, ws, 
     _check(lib().lora_apply(ctypes.byref(shape), _ptr(x), _ptr(y), _ptr(adapter_idx),
                             _ptr(A_stack), _ptr(B_stack), float(scale), _ptr(z), _ptr(ws),
                             _nbytes(ws), _stream(stream)), "lora_apply")
+
+
+def lora_shrink_noalloc(shape: Shape, x, A_stack, adapter_idx, scale, z, stream=None):
+    """lora_shrink with the library's built-in 4 MiB scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check(lib().lora_shrink_noalloc(ctypes.byref(shape), _ptr(x), _ptr(A_stack),
+                                     _ptr(adapter_idx), float(scale), _ptr(z), _stream(stream)),
+           "lora_shrink_noalloc")
 
 
 def check_status(ws, stream=None) -> int:
