@@ -193,9 +193,11 @@ class Stack:
         return n
 
 
-def make_shape(ig, st: Stack, mode, M=None):
+def make_shape(ig, st: Stack, mode, M=None, extra_flags=0):
+    # inference weights are never written while the step runs
     return ig.make_shape(st.M if M is None else M, st.K, st.N, st.r, slices=st.slices,
-                         num_adapters=st.L, split_k=WORKLOAD["S"], mode=mode)
+                         num_adapters=st.L, split_k=WORKLOAD["S"], mode=mode,
+                         flags=ig.FLAG_STATIC_WEIGHTS | extra_flags)
 
 
 def run_step(ig, st: Stack, sh, ws, M=None, stream=None):
@@ -207,7 +209,7 @@ def run_step(ig, st: Stack, sh, ws, M=None, stream=None):
     for l in range(st.layers):
         ig.lora_apply(sh, st.x[l][:M], st.y[l][:M], None, st.A[l], st.B[l], st.scale,
                       st.z[:, :M] if M == st.M else st.z_small[M], ws, stream)
-    return 1 + 2 * st.layers
+    return 1 + ig.plan_query(sh)["apply_kernels"] * st.layers
 
 
 def capture(ig, st, sh, ws, M=None):
@@ -242,25 +244,54 @@ def time_graph(g, steps, warmup, world, device):
     return max_over_ranks(ms, world, device)
 
 
-def kernel_durations(ig, st, sh, ws, reps=3):
-    """Average device duration of one shrink launch and one expand launch,
-    CUDA events around each launch on the launching stream."""
-    stream = torch.cuda.current_stream()
-    ig.map_tokens(sh, st.idx, ws)
-    ev = []
-    for _ in range(reps):
-        for l in range(st.layers):
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            e[0].record(stream)
-            ig.lora_shrink(sh, st.x[l], st.A[l], None, st.scale, st.z, ws)
-            e[1].record(stream)
-            ig.lora_expand(sh, st.z, st.B[l], None, st.y[l], ws)
-            e[2].record(stream)
-            ev.append(e)
+def kernel_durations(ig, st, ws, steps):
+    """Average device duration per launch of each kernel of the step: the
+    fused shrink+expand kernel (lora_apply, DET), and the two-kernel path's
+    Split-K shrink (counter protocol) and expand. Each is captured as
+    `layers` back-to-back launches (token map built once beforehand) in its
+    own CUDA graph and timed with CUDA events on the launching stream."""
+    fused = make_shape(ig, st, ig.MODE_DET)
+    two = make_shape(ig, st, ig.MODE_DET, extra_flags=ig.FLAG_UNFUSED)
+    ig.map_tokens(fused, st.idx, ws)
     torch.cuda.synchronize()
-    sh_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    ex_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    return sh_ms, ex_ms
+
+    def fused_only(stream):
+        for l in range(st.layers):
+            ig.lora_apply(fused, st.x[l], st.y[l], None, st.A[l], st.B[l], st.scale, st.z,
+                          ws, stream)
+
+    def shrink_only(stream):
+        for l in range(st.layers):
+            ig.lora_shrink(two, st.x[l], st.A[l], None, st.scale, st.z, ws, stream)
+
+    def expand_only(stream):
+        for l in range(st.layers):
+            ig.lora_expand(two, st.z, st.B[l], None, st.y[l], ws, stream)
+
+    out = {}
+    for name, fn in (("fused", fused_only), ("shrink", shrink_only), ("expand", expand_only)):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn(s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / (steps * st.layers)
+        del g
+    return out
 
 
 def source_hash(name):
@@ -401,6 +432,8 @@ def main():
     ws = {}
     for mode in (ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT):
         ws[mode] = ig.workspace(make_shape(ig, st, mode), device=device)
+    variants = (("det_sk8", ig.MODE_DET, 0), ("det_sk8_two_kernel", ig.MODE_DET, ig.FLAG_UNFUSED),
+                ("atomic_sk8", ig.MODE_ATOMIC, 0), ("unsplit_sk1", ig.MODE_UNSPLIT, 0))
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -409,11 +442,10 @@ def main():
     # main number: deterministic Split-K = 8
     results = {}
     graphs = {}
-    for mode, name in ((ig.MODE_DET, "det_sk8"), (ig.MODE_ATOMIC, "atomic_sk8"),
-                       (ig.MODE_UNSPLIT, "unsplit_sk1")):
-        sh = make_shape(ig, st, mode)
+    for name, mode, fl in variants:
+        sh = make_shape(ig, st, mode, extra_flags=fl)
         g, launches = capture(ig, st, sh, ws[mode])
-        graphs[mode] = (g, launches)
+        graphs[name] = (g, launches)
         ms = time_graph(g, args.steps, max(3, args.warmup), world, device)
         tok = W["M"] * W["layers"] * world / (ms * 1e-3)
         b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
@@ -430,6 +462,8 @@ def main():
     det = results["det_sk8"]
     results["det_overhead_vs_atomic_pct"] = 100 * (det["ms_per_step"] /
                                                    results["atomic_sk8"]["ms_per_step"] - 1)
+    results["det_two_kernel_overhead_vs_atomic_pct"] = 100 * (
+        results["det_sk8_two_kernel"]["ms_per_step"] / results["atomic_sk8"]["ms_per_step"] - 1)
     results["det_speedup_vs_unsplit_pct"] = 100 * (results["unsplit_sk1"]["ms_per_step"] /
                                                    det["ms_per_step"] - 1)
 
@@ -438,9 +472,8 @@ def main():
     if not args.no_sweep:
         for M in SWEEP_M:
             row = {}
-            for mode, name in ((ig.MODE_DET, "det"), (ig.MODE_ATOMIC, "atomic"),
-                               (ig.MODE_UNSPLIT, "unsplit")):
-                sh = make_shape(ig, st, mode, M=M)
+            for name, mode, fl in variants:
+                sh = make_shape(ig, st, mode, M=M, extra_flags=fl)
                 g, _ = capture(ig, st, sh, ws[mode], M=M)
                 ms = time_graph(g, max(20, args.steps // 4), 3, world, device)
                 u = int(torch.unique(st.idx[:M]).numel())
@@ -452,12 +485,14 @@ def main():
             sweep[str(M)] = row
 
     # dominant kernel roofline: per-launch CUDA-event durations
-    sh = make_shape(ig, st, ig.MODE_DET)
-    sh_ms, ex_ms = kernel_durations(ig, st, sh, ws[ig.MODE_DET])
+    kd = kernel_durations(ig, st, ws[ig.MODE_DET], max(20, args.steps // 4))
     b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
-    kern = {"shrink_fma (lora_shrink, det)": (sh_ms, b["shrink"], "shrink_fma.cu"),
-            "expand_fma (lora_expand)": (ex_ms, b["expand"], "expand_fma.cu")}
-    dom = max(kern, key=lambda k: kern[k][0])
+    kern = {"fused_fma (lora_apply, det)": (kd["fused"], b["total"], "fused_fma.cu"),
+            "shrink_fma (lora_shrink, det, two-kernel path)": (kd["shrink"], b["shrink"],
+                                                               "shrink_fma.cu"),
+            "expand_fma (lora_expand, two-kernel path)": (kd["expand"], b["expand"],
+                                                          "expand_fma.cu")}
+    dom = "fused_fma (lora_apply, det)"
     d_ms, d_bytes, d_file = kern[dom]
     achieved = d_bytes / (d_ms * 1e-3) / 1e9
     wkey = f"M={W['M']},K={W['K']},N={W['N']},r={W['r']},L={W['L']},S={W['S']}"
@@ -465,10 +500,11 @@ def main():
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": ncu_traffic(d_file, wkey),
                 "alg_bytes_per_launch": d_bytes, "us_per_launch": d_ms * 1e3,
-                "kernels_us_per_launch": {k: v[0] * 1e3 for k, v in kern.items()}}
+                "kernels": {k: {"us_per_launch": v[0] * 1e3, "alg_bytes": v[1],
+                                "gbs": v[1] / (v[0] * 1e-3) / 1e9} for k, v in kern.items()}}
 
     # end to end through the C ABI with host buffers (pinned), copies timed
-    g, launches = graphs[ig.MODE_DET]
+    g, launches = graphs["det_sk8"]
     hx = [t.cpu().pin_memory() for t in st.x]
     hy = [t.cpu().pin_memory() for t in st.y0]
     hidx = st.idx.cpu().pin_memory()

@@ -42,6 +42,13 @@
  *   - Return value: IG_OK, or a negative ig_status. Argument errors are
  *     detected on the host before anything is enqueued. IG_ERR_CUDA reports
  *     a failed launch (cudaGetLastError).
+ *   - Overlap: shrink and expand kernels are launched with programmatic
+ *     dependent launch. A kernel may start while the previous kernel on the
+ *     stream finishes, but it reads activations, z, y and the workspace
+ *     (other than the token map) and writes anything only after that kernel
+ *     has completed; only the token map (which is always complete before any
+ *     later kernel starts) and, with IG_FLAG_STATIC_WEIGHTS, A_stack/B_stack
+ *     are read earlier.
  *   - Determinism: in IG_MODE_DET and IG_MODE_UNSPLIT the bits of each z row
  *     and y row are a function of that row's inputs, its adapter and the plan
  *     only. The plan (ig_plan_query) is a function of
@@ -101,8 +108,21 @@ typedef struct ig_shape {
                            in IG_MODE_UNSPLIT */
   int32_t mode;         /* ig_mode */
   int32_t path;         /* ig_path */
-  int32_t reserved;     /* must be 0 */
+  int32_t flags;        /* 0 or IG_FLAG_* bits */
 } ig_shape;
+
+/* ig_shape.flags bits. */
+#define IG_FLAG_STATIC_WEIGHTS 1 /* A_stack and B_stack are not written by any
+                                    work still running on `stream` when the
+                                    call is enqueued (true for inference
+                                    weights). Lets a kernel start reading
+                                    them while the previous kernel on the
+                                    stream is still finishing. */
+#define IG_FLAG_UNFUSED 2        /* lora_apply in IG_MODE_DET runs the Split-K
+                                    shrink (counter protocol, Algorithm 1)
+                                    and the expand as two kernels even where
+                                    the fused one-launch kernel applies. Both
+                                    give the same bits. */
 
 /* The resolved plan. Everything that fixes the arithmetic is in
  * determinism_key, which never depends on M. */
@@ -118,6 +138,11 @@ typedef struct ig_plan_info {
   int64_t shrink_ctas_max;  /* shrink grid size for this M */
   int64_t workspace_bytes;  /* same as ig_workspace_bytes */
   uint64_t determinism_key; /* hash of the arithmetic-defining plan fields */
+  int32_t apply_kernels;    /* kernels lora_apply launches after the token
+                               map: 1 = fused shrink+expand (IG_MODE_DET,
+                               r = 8 or 16, S <= 16, FMA path), 2 = shrink
+                               then expand */
+  int32_t reserved;
 } ig_plan_info;
 
 /* Library version string and a message for a status code. Host only. */
@@ -173,7 +198,12 @@ int lora_expand(const ig_shape* shape, const float* z, const void* B_stack,
 
 /* Token map (if adapter_idx != NULL), shrink into z, then expand into y, all
  * on `stream`. z is caller-owned scratch of slices*M*r floats and holds the
- * shrink output afterwards. */
+ * shrink output afterwards. In IG_MODE_DET with r = 8 or 16 and S <= 16 the
+ * shrink and expand run as one launch: the S partition blocks of a tile form
+ * a thread-block cluster, sum their partials over distributed shared memory
+ * in the same increasing partition order, and expand the tile's rows
+ * (ig_plan_info.apply_kernels == 1; IG_FLAG_UNFUSED turns this off). The
+ * results are bit-identical to the two-kernel sequence. */
 int lora_apply(const ig_shape* shape, const void* x, void* y,
                const int32_t* adapter_idx, const void* A_stack,
                const void* B_stack, float scale, float* z,

@@ -20,6 +20,7 @@ import os
 
 __all__ = [
     "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "PATH_AUTO", "PATH_FMA", "PATH_MMA",
+    "FLAG_STATIC_WEIGHTS", "FLAG_UNFUSED",
     "IGError", "Shape", "PlanInfo", "lib", "lib_path", "make_shape", "workspace_bytes",
     "plan_query", "workspace", "workspace_init", "map_tokens", "lora_shrink",
     "lora_expand", "lora_apply", "lora_shrink_noalloc", "check_status", "status_string",
@@ -27,6 +28,8 @@ __all__ = [
 ]
 
 MODE_DET, MODE_ATOMIC, MODE_UNSPLIT = 0, 1, 2
+FLAG_STATIC_WEIGHTS = 1
+FLAG_UNFUSED = 2
 PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 
 STATUS = {
@@ -60,7 +63,7 @@ class Shape(ctypes.Structure):
         ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("N", ctypes.c_int64),
         ("r", ctypes.c_int64), ("slices", ctypes.c_int32), ("num_adapters", ctypes.c_int32),
         ("split_k", ctypes.c_int32), ("mode", ctypes.c_int32), ("path", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
     ]
 
 
@@ -71,6 +74,7 @@ class PlanInfo(ctypes.Structure):
         ("expand_bm", ctypes.c_int32), ("expand_bn", ctypes.c_int32),
         ("shrink_tiles_max", ctypes.c_int64), ("shrink_ctas_max", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64), ("determinism_key", ctypes.c_uint64),
+        ("apply_kernels", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -123,9 +127,9 @@ def status_string(code: int) -> str:
 
 
 def make_shape(M, K, N, r, *, slices=1, num_adapters=1, split_k=8, mode=MODE_DET,
-               path=PATH_AUTO) -> Shape:
+               path=PATH_AUTO, flags=0) -> Shape:
     return Shape(int(M), int(K), int(N), int(r), int(slices), int(num_adapters),
-                 int(split_k), int(mode), int(path), 0)
+                 int(split_k), int(mode), int(path), int(flags))
 
 
 def _ptr(t):

@@ -17,10 +17,10 @@ struct Plan {
   int64_t Ks;        // K / S
   int bn;            // shrink rank columns per tile
   int jblocks;       // r / bn
-  int64_t tiles;     // shrink tiles upper bound (groups 0..L)
-  int64_t etiles;    // expand tiles upper bound (groups 0..L-1)
+  int64_t tiles;     // tile-table entries: upper bound on tiles (groups 0..L)
   int ntiles;        // expand column tiles per slice
-  size_t off_perm, off_offsets, off_partials, total;
+  size_t off_perm, off_offsets, off_tiles, off_partials, total;
+  bool fused;        // lora_apply runs the one-launch cluster kernel
   uint64_t key;
 };
 
@@ -34,7 +34,7 @@ uint64_t fnv1a(uint64_t h, int64_t v) {
 
 int make_plan(const ig_shape* sh, Plan* pl) {
   if (!sh || !pl) return IG_ERR_ARG;
-  if (sh->reserved != 0) return IG_ERR_ARG;
+  if ((sh->flags & ~(IG_FLAG_STATIC_WEIGHTS | IG_FLAG_UNFUSED)) != 0) return IG_ERR_ARG;
   if (sh->mode < IG_MODE_DET || sh->mode > IG_MODE_UNSPLIT) return IG_ERR_ARG;
   if (sh->path < IG_PATH_AUTO || sh->path > IG_PATH_MMA) return IG_ERR_ARG;
   const int64_t M = sh->M, K = sh->K, N = sh->N, r = sh->r;
@@ -58,22 +58,26 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   pl->bn = (r % 16 == 0) ? 16 : 8;
   pl->jblocks = (int)(r / pl->bn);
   const int L = sh->num_adapters;
-  pl->tiles = tiles_upper_bound(M, L + 1, kShrinkBM);
-  pl->etiles = tiles_upper_bound(M, L, kExpandBM);
+  pl->tiles = tiles_upper_bound(M, L + 1, kTileRows);
   pl->ntiles = (int)((N + kExpandBN - 1) / kExpandBN);
   const int64_t slots = pl->tiles * sh->slices * pl->jblocks;
   if (sh->mode == IG_MODE_DET && slots > kMaxCounters) return IG_ERR_UNSUPPORTED;
 
   pl->off_perm = kMapOffset;
   pl->off_offsets = align_up(pl->off_perm + 4 * (size_t)M, 256);
-  pl->off_partials = align_up(pl->off_offsets + 4 * (size_t)(L + 2), 256);
+  pl->off_tiles = align_up(pl->off_offsets + 4 * (size_t)(L + 2), 256);
+  pl->off_partials = align_up(pl->off_tiles + 4 * (size_t)kTileInts * pl->tiles, 256);
   size_t part = 0;
-  if (sh->mode == IG_MODE_DET) part = (size_t)slots * S * kShrinkBM * pl->bn * sizeof(float);
+  if (sh->mode == IG_MODE_DET) part = (size_t)slots * S * kTileRows * pl->bn * sizeof(float);
   pl->total = align_up(pl->off_partials + part, 256);
+
+  pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_FMA && (r == 8 || r == 16) &&
+              pl->bn == r && S <= 16 && !(sh->flags & IG_FLAG_UNFUSED) &&
+              fused_smem_bytes(pl->bn, pl->Ks, N, S) <= 200 * 1024;
 
   uint64_t h = 1469598103934665603ull;
   const int64_t fields[] = {IG_ABI_VERSION, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
-                            pl->bn, kShrinkKB, kShrinkRowsPerWarp, kExpandJC};
+                            pl->bn, kShrinkKB};
   for (int64_t f : fields) h = fnv1a(h, f);
   pl->key = h;
   return IG_OK;
@@ -99,8 +103,10 @@ int run_map(const ig_shape* sh, const Plan& pl, const int32_t* idx, uint8_t* ws,
   mp.idx = idx;
   mp.perm = reinterpret_cast<int32_t*>(ws + pl.off_perm);
   mp.offsets = reinterpret_cast<int32_t*>(ws + pl.off_offsets);
+  mp.tiles = reinterpret_cast<int32_t*>(ws + pl.off_tiles);
   mp.status = reinterpret_cast<uint32_t*>(ws);
   mp.M = sh->M;
+  mp.tiles_max = pl.tiles;
   mp.L = sh->num_adapters;
   return cuda_status(launch_map_tokens(mp, st));
 }
@@ -114,8 +120,7 @@ int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
   ShrinkParams p;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.A = static_cast<const __nv_bfloat16*>(A);
-  p.perm = reinterpret_cast<const int32_t*>(ws + pl.off_perm);
-  p.offsets = reinterpret_cast<const int32_t*>(ws + pl.off_offsets);
+  p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
   p.z = z;
   p.partials = reinterpret_cast<float*>(ws + pl.off_partials);
   p.counters = reinterpret_cast<uint32_t*>(ws + kCountersOffset);
@@ -128,8 +133,31 @@ int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
   p.L = sh->num_adapters;
   p.S = pl.S;
   p.jblocks = pl.jblocks;
+  p.flags = sh->flags;
   p.scale = scale;
   return cuda_status(launch_shrink_fma(p, pl.mode, pl.bn, pl.tiles, st));
+}
+
+int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, const void* B,
+              float scale, float* z, void* y, uint8_t* ws, cudaStream_t st) {
+  FusedParams p;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.A = static_cast<const __nv_bfloat16*>(A);
+  p.B = static_cast<const __nv_bfloat16*>(B);
+  p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
+  p.z = z;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.M = sh->M;
+  p.K = sh->K;
+  p.N = sh->N;
+  p.Ks = pl.Ks;
+  p.slices = sh->slices;
+  p.L = sh->num_adapters;
+  p.S = pl.S;
+  p.flags = sh->flags;
+  p.scale = scale;
+  return cuda_status(launch_fused_fma(p, pl.bn, pl.tiles, st));
 }
 
 int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
@@ -137,8 +165,7 @@ int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B
   ExpandParams p;
   p.z = z;
   p.B = static_cast<const __nv_bfloat16*>(B);
-  p.perm = reinterpret_cast<const int32_t*>(ws + pl.off_perm);
-  p.offsets = reinterpret_cast<const int32_t*>(ws + pl.off_offsets);
+  p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.M = sh->M;
@@ -147,7 +174,8 @@ int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B
   p.slices = sh->slices;
   p.L = sh->num_adapters;
   p.ntiles = pl.ntiles;
-  return cuda_status(launch_expand_fma(p, pl.etiles, st));
+  p.flags = sh->flags;
+  return cuda_status(launch_expand_fma(p, pl.tiles, st));
 }
 
 }  // namespace
@@ -190,7 +218,7 @@ int ig_plan_query(const ig_shape* shape, ig_plan_info* out) {
   out->path = pl.path;
   out->split_k = pl.S;
   out->k_split = pl.Ks;
-  out->shrink_bm = kShrinkBM;
+  out->shrink_bm = kTileRows;
   out->shrink_bn = pl.bn;
   out->expand_bm = kExpandBM;
   out->expand_bn = kExpandBN;
@@ -198,6 +226,7 @@ int ig_plan_query(const ig_shape* shape, ig_plan_info* out) {
   out->shrink_ctas_max = pl.tiles * shape->slices * pl.jblocks * pl.S;
   out->workspace_bytes = (int64_t)pl.total;
   out->determinism_key = pl.key;
+  out->apply_kernels = pl.fused ? 1 : 2;
   return IG_OK;
 }
 
@@ -287,6 +316,7 @@ int lora_apply(const ig_shape* shape, const void* x, void* y, const int32_t* ada
     rc = run_map(shape, pl, adapter_idx, w, st);
     if (rc != IG_OK) return rc;
   }
+  if (pl.fused) return run_fused(shape, pl, x, A_stack, B_stack, scale, z, y, w, st);
   rc = run_shrink(shape, pl, x, A_stack, scale, z, w, st);
   if (rc != IG_OK) return rc;
   return run_expand(shape, pl, z, B_stack, y, w, st);

@@ -1,0 +1,307 @@
+// Fused decode LoRA layer: deterministic Split-K shrink and expand in one
+// launch, with the S partition blocks of a tile forming one thread-block
+// cluster.
+//
+// "Reproducible LoRA Inference Through Deterministic Split-K Reduction",
+// sec. 4.3 / Algorithm 1 / Fig. 2: S blocks compute FP32 partials of one
+// output tile, and the partials are summed in increasing partition order
+// starting from FP32 zero, then multiplied by the scale. The pages keep the
+// partials in global scratch and pick the block that finishes last with an
+// integer counter, and they run the expand as a separate kernel; they name
+// the extra launch as the cost of the earlier two-kernel design (sec. 4.3)
+// and leave the expand to vLLM (Eq. 1). On GB300 the S blocks of a tile can
+// be one cluster: each block keeps its partial in its own shared memory, a
+// cluster barrier publishes them, and every block reads all S partials over
+// distributed shared memory in the same fixed order. No scratch, no
+// counter, and the expand of the tile's rows follows in the same launch,
+// each block taking 1/S of the output columns.
+//
+// Bit-for-bit the same results as the two-kernel path (shrink kernel with
+// the counter protocol, then the expand kernel): the partials come from the
+// same code (shrink_core.cuh), the combine adds them in the same order, and
+// the expand keeps the same j order and single rounding.
+//
+// Block = 16/RPW warps of RPW = 32/r rows; cluster = S blocks (rank s = K
+// partition s); tile = up to 16 token rows of one adapter (tile-table entry)
+// x all r rank columns (r = 8 or 16). Shared memory: the x/A ring of the shrink, the block's
+// partial, the tile's bf16-rounded Z, the block's B column slice (bulk
+// copies, padded for conflict-free reads) and the tile's y rows for those
+// columns (bulk copies, issued right after griddep_wait so they arrive while
+// the shrink computes).
+#include "shrink_core.cuh"
+
+namespace ig {
+
+namespace {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+struct FusedLayout {
+  int nst;           // ring depth
+  int cols;          // output columns per block (multiple of 8)
+  size_t ring_off, part_off, zs_off, b_off, y_off, bytes;
+};
+
+template <int BN>
+__host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S) {
+  FusedLayout L;
+  const int nkb = (int)((Ks + kShrinkKB - 1) / kShrinkKB);
+  L.nst = nkb < kShrinkStages ? nkb : kShrinkStages;
+  L.cols = (int)(((N + S - 1) / S + 7) / 8 * 8);
+  L.ring_off = 256;
+  L.part_off = L.ring_off + (size_t)L.nst * PartialRing<BN>::kStageBytes;
+  L.zs_off = L.part_off + kTileRows * BN * 4;
+  L.b_off = L.zs_off + kTileRows * BN * 4;
+  L.y_off = L.b_off + (size_t)(L.cols / 8) * (16 * BN + 16);
+  L.bytes = L.y_off + (size_t)kTileRows * L.cols * 2;
+  return L;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(FusedParams p) {
+  constexpr int kThreads = ShrinkGeo<BN>::THREADS;
+  constexpr int RPW = ShrinkGeo<BN>::RPW;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const FusedLayout lay = fused_layout<BN>(p.Ks, p.N, p.S);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // ring bars [0, 4)
+  uint64_t* bar_by = bars + kShrinkStages;                       // B and y copies
+  int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);        // tile entry
+  float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [16][BN]
+  float* zs = reinterpret_cast<float*>(smem + lay.zs_off);       // [16][BN]
+  uint8_t* sB = smem + lay.b_off;
+  uint8_t* sY = smem + lay.y_off;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.S;
+  const int s = (int)cluster_rank();
+  const int64_t cl = blockIdx.x / S;
+  const int sl = (int)(cl % p.slices);
+  const int64_t t = cl / p.slices;
+
+  if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
+  if (tid == 0) {
+    for (int i = 0; i < lay.nst; ++i) mbar_init(&bars[i], 1);
+    mbar_init(bar_by, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int g = ent_s[0];
+  const int nrows = ent_s[1];
+  const int32_t* rows_s = ent_s + 4;
+  const int64_t M = p.M, N = p.N, K = p.K;
+  const int r = BN;
+  if (nrows <= 0) return;  // the whole cluster shares the tile: all exit
+
+  if (g == p.L) {
+    // tokens without an adapter: zero Z rows, y untouched
+    griddep_wait();
+    griddep_launch();
+    if (s == 0)
+      for (int i = tid; i < nrows * r; i += kThreads)
+        p.z[((int64_t)sl * M + rows_s[i / r]) * r + i % r] = 0.0f;
+    return;
+  }
+
+  // this block's output columns [c0, c0 + ncols) of slice sl
+  const int64_t c0 = (int64_t)s * lay.cols;
+  const int ncols = (int)max((int64_t)0, min((int64_t)lay.cols, N - c0));
+  const int groups = ncols / 8;
+  const int lbs = 16 * r + 16;
+  const bool early_w = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
+
+  PartialArgs pa;
+  pa.x = p.x + (int64_t)s * p.Ks;
+  pa.A = p.A + ((int64_t)g * p.slices + sl) * r * K + (int64_t)s * p.Ks;
+  pa.rows = rows_s;
+  pa.status = p.status;
+  pa.K = K;
+  pa.Ks = p.Ks;
+  pa.nrows = nrows;
+  PartialRing<BN> ring;
+  ring.stages = smem + lay.ring_off;
+  ring.bars = bars;
+  ring.nst = lay.nst;
+  ring.nkb = (int)((p.Ks + kShrinkKB - 1) / kShrinkKB);
+  const int first = min(ring.nkb, lay.nst);
+
+  const __nv_bfloat16* Bsrc = p.B + (((int64_t)g * p.slices + sl) * N + c0) * r;
+  auto issue_b = [&]() {
+    for (int q = lane; q < groups; q += 32)
+      bulk_g2s(sB + q * lbs, Bsrc + (int64_t)q * 8 * r, 16 * r, bar_by);
+  };
+  const int64_t ldy = (int64_t)p.slices * N;
+  auto issue_y = [&]() {
+    if (ncols > 0)
+      for (int i = lane; i < nrows; i += 32)
+        bulk_g2s(sY + i * ncols * 2, p.y + (int64_t)rows_s[i] * ldy + (int64_t)sl * N + c0,
+                 (uint32_t)ncols * 2, bar_by);
+  };
+
+  if (warp == 0) {
+    if (lane == 0)
+      mbar_arrive_expect_tx(bar_by, (uint32_t)groups * 16 * r + (uint32_t)nrows * ncols * 2);
+    __syncwarp();
+    for (int b = 0; b < first; ++b) {
+      ring.expect(pa, b);
+      if (early_w) ring.issue_a(pa, b);
+    }
+    if (early_w) issue_b();
+  }
+  griddep_wait();
+  griddep_launch();
+  if (warp == 0) {
+    for (int b = 0; b < first; ++b) {
+      if (!early_w) ring.issue_a(pa, b);
+      ring.issue_x(pa, b);
+    }
+    if (!early_w) issue_b();
+    issue_y();
+  }
+
+  float v;
+  const bool ok = ring.run(pa, v);
+  part[(warp * RPW + lane / BN) * BN + lane % BN] = ok ? v : 0.0f;
+
+  // Every block of the cluster reaches both cluster barriers on every path.
+  cluster_sync();  // all partials written and visible across the cluster
+
+  // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
+  for (int o = tid; o < nrows * BN; o += kThreads) {
+    float total = 0.0f;
+    for (int q = 0; q < S; ++q) total += ld_dsmem_f32(part + o, (uint32_t)q);
+    const float zv = total * p.scale;
+    zs[o] = bf16_round_f32(zv);
+    if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
+  }
+  cluster_arrive();  // done reading the other blocks' partials
+  __syncthreads();   // zs complete
+
+  // Expand this block's columns: y = bf16_rn(f32(y) + sum_j zb_j B_nj), the
+  // j sum a chain of FMAs in increasing j (two columns per f32x2 FMA).
+  const bool copies_ok = mbar_wait_bounded(bar_by, 0, p.status);
+  const int row0 = warp * RPW;
+  if (copies_ok && row0 < nrows) {
+    float2 zz[RPW][BN];  // this warp's Z rows, each value in both halves
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+      for (int j = 0; j < BN; ++j) {
+        const float zv = (row0 + rr < nrows) ? zs[(row0 + rr) * BN + j] : 0.0f;
+        zz[rr][j] = make_float2(zv, zv);
+      }
+    for (int q = lane; q < groups; q += 32) {  // this lane's 8-column group
+      float2 acc[RPW][4];
+#pragma unroll
+      for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) acc[rr][cp] = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int cp = 0; cp < 4; ++cp) {
+#pragma unroll
+        for (int h = 0; h < BN / 8; ++h) {
+          const uint4 u0 =
+              *reinterpret_cast<const uint4*>(sB + q * lbs + ((2 * cp) * r + 8 * h) * 2);
+          const uint4 u1 =
+              *reinterpret_cast<const uint4*>(sB + q * lbs + ((2 * cp + 1) * r + 8 * h) * 2);
+          float b0[8], b1[8];
+          unpack8(u0, b0);
+          unpack8(u1, b1);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 bb = make_float2(b0[e], b1[e]);
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr)
+              acc[rr][cp] = __ffma2_rn(zz[rr][8 * h + e], bb, acc[rr][cp]);
+          }
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < RPW; ++rr) {
+        const int row = row0 + rr;
+        if (row >= nrows) break;
+        const uint4 yu = *reinterpret_cast<const uint4*>(sY + (row * ncols + q * 8) * 2);
+        float yf[8];
+        unpack8(yu, yf);
+        uint32_t o[8];
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {
+          o[2 * cp] = f32_to_bf16_bits(yf[2 * cp] + acc[rr][cp].x);
+          o[2 * cp + 1] = f32_to_bf16_bits(yf[2 * cp + 1] + acc[rr][cp].y);
+        }
+        uint4 w;
+        w.x = o[0] | (o[1] << 16);
+        w.y = o[2] | (o[3] << 16);
+        w.z = o[4] | (o[5] << 16);
+        w.w = o[6] | (o[7] << 16);
+        *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[row] * ldy + (int64_t)sl * N + c0 +
+                                  q * 8) = w;
+      }
+    }
+  }
+  // a copy that never completed: wait for it once more (bounded) before the
+  // block's shared memory goes away
+  if (!copies_ok) mbar_wait_bounded(bar_by, 0, p.status);
+  cluster_wait();  // no block leaves while another may still read its partial
+}
+
+}  // namespace
+
+size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S) {
+  return bn == 16 ? fused_layout<16>(Ks, N, S).bytes : fused_layout<8>(Ks, N, S).bytes;
+}
+
+cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st) {
+  const int64_t grid = tiles_max * p.slices * p.S;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const size_t smem = fused_smem_bytes(bn, p.Ks, p.N, p.S);
+  void (*kern)(FusedParams) = bn == 16 ? fused_fma_kernel<16> : fused_fma_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  if (p.S > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(bn == 16 ? ShrinkGeo<16>::THREADS : ShrinkGeo<8>::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace ig

@@ -18,8 +18,9 @@ namespace ig {
 //
 //   [0, 256)                      status words (u32 status at offset 0)
 //   [256, 256 + 4*kMaxCounters)   per-tile completion counters (u32)
-//   [kMapOffset, ...)             token map: perm[M] int32, then
-//                                 offsets[G+1] int32 at a 256-byte boundary
+//   [kMapOffset, ...)             token map: perm[M] int32, offsets[G+1]
+//                                 int32, tile table [tiles_max][kTileInts]
+//                                 int32 (each at a 256-byte boundary)
 //   [partials, ...)               FP32 partials [slots][S][BM*BN] (DET only)
 //
 // The counters sit at a fixed place whatever the shape, so one
@@ -40,17 +41,18 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) {
   return (v + a - 1) / a * a;
 }
 
-// FMA-path tile geometry (fixed: part of the determinism key).
-constexpr int kShrinkWarps = 8;
-constexpr int kShrinkRowsPerWarp = 4;
-constexpr int kShrinkBM = kShrinkWarps * kShrinkRowsPerWarp;  // 32 token rows
+// FMA-path geometry (fixed: part of the determinism key where it sets the
+// arithmetic order).
+constexpr int kTileRows = 16;          // token rows per tile of the tile table
+constexpr int kTileInts = 4 + kTileRows;  // [g, nrows, 0, 0, rows[16]] = 80 bytes
 constexpr int kShrinkKB = 256;        // elements per k-block: 32 lanes x 8
 constexpr int kShrinkStages = 4;
 constexpr int kExpandWarps = 8;
-constexpr int kExpandRowsPerWarp = 4;
-constexpr int kExpandBM = kExpandWarps * kExpandRowsPerWarp;  // 32 token rows
+constexpr int kExpandRowsPerWarp = 2;
+constexpr int kExpandBM = kExpandWarps * kExpandRowsPerWarp;  // 16 = kTileRows
 constexpr int kExpandBN = 256;        // output columns: 32 lanes x 8
-constexpr int kExpandJC = 8;          // rank elements per register chunk
+constexpr int kExpandJC = 16;         // rank elements per register chunk
+static_assert(kExpandBM == kTileRows, "tile rows");
 
 // Tile count over token groups: sum over groups g of ceil(count_g / bm),
 // bounded by floor(M / bm) + (number of non-empty groups).
@@ -64,34 +66,47 @@ struct MapParams {
   const int32_t* idx;
   int32_t* perm;
   int32_t* offsets;
+  int32_t* tiles;      // tile table [tiles_max][kTileInts]
   uint32_t* status;
   int64_t M;
+  int64_t tiles_max;
   int32_t L;
 };
 
 struct ShrinkParams {
   const __nv_bfloat16* x;
   const __nv_bfloat16* A;
-  const int32_t* perm;
-  const int32_t* offsets;
+  const int32_t* tiles;
   float* z;
   float* partials;
   uint32_t* counters;
   uint32_t* status;
   int64_t M, K, r, Ks;
-  int32_t slices, L, S, jblocks;
+  int32_t slices, L, S, jblocks, flags;
   float scale;
 };
 
 struct ExpandParams {
   const float* z;
   const __nv_bfloat16* B;
-  const int32_t* perm;
-  const int32_t* offsets;
+  const int32_t* tiles;
   __nv_bfloat16* y;
   uint32_t* status;
   int64_t M, N, r;
-  int32_t slices, L, ntiles;
+  int32_t slices, L, ntiles, flags;
+};
+
+struct FusedParams {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* A;
+  const __nv_bfloat16* B;
+  const int32_t* tiles;
+  float* z;
+  __nv_bfloat16* y;
+  uint32_t* status;
+  int64_t M, K, N, Ks;
+  int32_t slices, L, S, flags;
+  float scale;
 };
 
 // Launchers (defined in the .cu files); they return cudaGetLastError().
@@ -100,6 +115,27 @@ cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn,
                               int64_t tiles_max, cudaStream_t st);
 cudaError_t launch_expand_fma(const ExpandParams& p, int64_t tiles_max,
                               cudaStream_t st);
+cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st);
+size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S);
+
+// Launch helper: programmatic dependent launch on `st` (see griddep_wait).
+template <typename Kern, typename P>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const P& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 #ifdef __CUDACC__
 // ---------------------------------------------------------------------------
@@ -122,6 +158,19 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
 }
 __device__ __forceinline__ float bf16_round_f32(float f) {
   return __uint_as_float(f32_to_bf16_bits(f) << 16);
+}
+
+// Programmatic dependent launch. A kernel launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization may start before the
+// previous kernel on the stream has finished; griddep_wait() blocks until that
+// kernel has completed and its memory is visible. Every kernel here reads
+// activations, z, y and workspace state, and writes anything, only after
+// griddep_wait(). griddep_launch() lets the next kernel start launching.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -172,6 +221,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// Ask for `bytes` (a multiple of 16, from a 16-byte aligned address) to be
+// brought into L2; no destination, no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
@@ -179,41 +234,6 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
   return old;
 }
 
-// Locate output tile `t` among token groups [0, G): group g holds rows
-// offsets[g] .. offsets[g+1]-1 of the permuted order and ceil(count/bm)
-// tiles. Called by one full warp; every lane gets the result. Returns false
-// when t is past the last tile.
-__device__ __forceinline__ bool find_tile(const int32_t* offsets, int G, int bm, int64_t t,
-                                          int* g_out, int* row0_out, int* nrows_out) {
-  const int lane = threadIdx.x & 31;
-  int64_t before = 0;
-  for (int base = 0; base < G; base += 32) {
-    const int g = base + lane;
-    int cnt = 0;
-    if (g < G) cnt = offsets[g + 1] - offsets[g];
-    int64_t tl = (cnt + bm - 1) / bm;
-    int64_t incl = tl;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
-    if (t < before + total) {
-      const unsigned hit = __ballot_sync(0xffffffffu, t < before + incl);
-      const int src = __ffs(hit) - 1;
-      const int64_t excl = __shfl_sync(0xffffffffu, incl - tl, src);
-      const int c = __shfl_sync(0xffffffffu, cnt, src);
-      const int q = (int)(t - before - excl);
-      *g_out = base + src;
-      *row0_out = q * bm;
-      *nrows_out = min(bm, c - q * bm);
-      return true;
-    }
-    before += total;
-  }
-  return false;
-}
 #endif  // __CUDACC__
 
 }  // namespace ig

@@ -16,6 +16,17 @@
 // into global start positions (exclusive scan over warps, then over groups);
 // pass 2 re-walks the segments and writes each row to
 // start[warp][g] + (rank among equal groups within the 32-row step).
+//
+// Finally it writes the tile table the shrink and expand kernels read: group
+// g is cut into ceil(count_g / 16) tiles of at most 16 consecutive rows of
+// the grouped order; tile entries hold [g, nrows, 0, 0, rows[16]] so that a
+// block learns its adapter and its token rows with one 80-byte load. Tiles of
+// adapters 0..L-1 come first (in adapter order), then the no-adapter group,
+// then empty entries (nrows = 0) up to tiles_max.
+//
+// This kernel is launched without programmatic dependent launch and never
+// releases its dependents early, so every later kernel on the stream starts
+// after the map is complete and may read it before its own griddep_wait().
 #include "ig_common.cuh"
 
 namespace ig {
@@ -33,9 +44,11 @@ __device__ __forceinline__ int group_of(const int32_t* idx, int64_t m, int L, ui
 }
 
 __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
-  extern __shared__ int32_t hist[];  // [kMapWarps][G], then total[G]
+  extern __shared__ int32_t hist[];  // [kMapWarps][G], total[G], cntg[G], tstart[G+1]
   const int G = p.L + 1;
   int32_t* total = hist + kMapWarps * G;
+  int32_t* cntg = total + G;
+  int32_t* tstart = cntg + G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t M = p.M;
   const int64_t seg = (M + kMapWarps - 1) / kMapWarps;
@@ -86,6 +99,7 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
         if (lane >= o) incl += v;
       }
       if (g < G) {
+        cntg[g] = c;
         total[g] = carry + incl - c;  // now the group's start
         p.offsets[g] = carry + incl - c;
       }
@@ -95,6 +109,24 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
   }
   __syncthreads();
 
+  // tile starts per group: exclusive scan of ceil(count_g / kTileRows)
+  __syncthreads();
+  if (warp == 0) {
+    int32_t carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      const int32_t c = g < G ? (cntg[g] + kTileRows - 1) / kTileRows : 0;
+      int32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < G) tstart[g] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tstart[G] = carry;
+  }
   for (int i = tid; i < kMapWarps * G; i += kMapThreads) hist[i] += total[i % G];
   __syncthreads();
 
@@ -117,13 +149,37 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
     }
     __syncwarp();
   }
+  __syncthreads();
+
+  // tile table: one warp per tile, lane i < 16 writes row i
+  const int64_t ntiles = tstart[G];
+  for (int64_t t = warp; t < p.tiles_max; t += kMapWarps) {
+    int32_t* ent = p.tiles + t * kTileInts;
+    if (t >= ntiles) {
+      if (lane < kTileInts) ent[lane] = lane == 0 ? -1 : 0;
+      continue;
+    }
+    int lo_g = 0, hi_g = G - 1;  // last group with tstart[g] <= t
+    while (lo_g < hi_g) {
+      const int mid = (lo_g + hi_g + 1) >> 1;
+      if (tstart[mid] <= t) lo_g = mid; else hi_g = mid - 1;
+    }
+    const int g = lo_g;
+    const int q = (int)(t - tstart[g]);
+    const int first = total[g] + q * kTileRows;          // total[] holds group starts
+    const int cnt = min(kTileRows, total[g] + cntg[g] - first);
+    if (lane == 0) ent[0] = g;
+    if (lane == 1) ent[1] = cnt;
+    if (lane == 2 || lane == 3) ent[lane] = 0;
+    if (lane < kTileRows) ent[4 + lane] = lane < cnt ? p.perm[first + lane] : 0;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_map_tokens(const MapParams& p, cudaStream_t st) {
   const int G = p.L + 1;
-  const size_t smem = (size_t)(kMapWarps + 1) * G * sizeof(int32_t);
+  const size_t smem = ((size_t)(kMapWarps + 3) * G + 1) * sizeof(int32_t);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(map_tokens_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

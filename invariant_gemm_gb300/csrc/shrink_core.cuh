@@ -1,0 +1,181 @@
+// The shrink partial of one tile over one K partition, on CUDA cores. Shared
+// by the Split-K shrink kernel and the fused decode kernel so that both
+// compute bit-identical partials.
+//
+// Tile: up to 16 token rows x BN rank columns (BN = 8 or 16). The block has
+// 16/RPW warps of RPW = 32/BN rows each, so every lane ends with exactly one
+// finished output. The partition [k0, k0 + Ks) is streamed through a ring of
+// `nst` shared-memory stages, k-blocks of 256 elements, by 1-D bulk async
+// copies: one per token row (x) and one per rank column (A), completion
+// counted in bytes on one mbarrier per stage. Warp 0 issues the copies.
+//
+// Order of the sum, identical for every row and every M ("Reproducible LoRA
+// Inference Through Deterministic Split-K Reduction" leaves the order inside
+// a partition to the kernel, sec. 4.3): lane l owns the 8-element chunks
+// l, l+32, ... of the partition and accumulates them in increasing k with FMA
+// (two independent FMAs per packed f32x2 instruction, each rounded like
+// fmaf); the 32 lane sums are then combined by a fixed xor butterfly
+// (16, 8, 4, 2, 1) as a reduce-scatter. Neither the number of rows a warp
+// holds nor which warp holds a row changes a row's arithmetic.
+#pragma once
+
+#include "ig_common.cuh"
+
+namespace ig {
+
+template <int BN>
+struct ShrinkGeo {
+  static constexpr int RPW = 32 / BN;             // rows per warp
+  static constexpr int WARPS = kTileRows / RPW;   // 8 for BN = 16, 4 for BN = 8
+  static constexpr int THREADS = WARPS * 32;
+  static_assert(RPW * BN == 32 && WARPS * RPW == kTileRows, "shrink geometry");
+};
+
+struct PartialArgs {
+  const __nv_bfloat16* x;     // x + k0
+  const __nv_bfloat16* A;     // first A row of the tile's column block, + k0
+  const int32_t* rows;        // token rows of the tile (shared memory)
+  uint32_t* status;
+  int64_t K;                  // row stride of x and A, in elements
+  int64_t Ks;                 // partition length
+  int nrows;
+};
+
+template <int BN>
+struct PartialRing {
+  using G = ShrinkGeo<BN>;
+  static constexpr int kRowBytes = kShrinkKB * 2;                  // 512
+  static constexpr int kStageBytes = (kTileRows + BN) * kRowBytes;
+  uint8_t* stages;
+  uint64_t* bars;
+  int nst;      // ring depth
+  int nkb;      // k-blocks in the partition
+
+  __device__ __forceinline__ uint32_t block_bytes(const PartialArgs& a, int b) const {
+    return (uint32_t)(min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB) * 2);
+  }
+  // warp 0: arm stage b % nst for all copies of k-block b
+  __device__ __forceinline__ void expect(const PartialArgs& a, int b) const {
+    if ((threadIdx.x & 31) == 0)
+      mbar_arrive_expect_tx(&bars[b % nst], block_bytes(a, b) * (uint32_t)(a.nrows + BN));
+    __syncwarp();
+  }
+  __device__ __forceinline__ void issue_a(const PartialArgs& a, int b) const {
+    const int lane = threadIdx.x & 31;
+    const int st = b % nst;
+    const uint32_t bytes = block_bytes(a, b);
+    uint8_t* sa = stages + st * kStageBytes + kTileRows * kRowBytes;
+    for (int j = lane; j < BN; j += 32)
+      bulk_g2s(sa + j * kRowBytes, a.A + (int64_t)j * a.K + (int64_t)b * kShrinkKB, bytes,
+               &bars[st]);
+  }
+  __device__ __forceinline__ void issue_x(const PartialArgs& a, int b) const {
+    const int lane = threadIdx.x & 31;
+    const int st = b % nst;
+    const uint32_t bytes = block_bytes(a, b);
+    uint8_t* sx = stages + st * kStageBytes;
+    for (int i = lane; i < a.nrows; i += 32)
+      bulk_g2s(sx + i * kRowBytes, a.x + (int64_t)a.rows[i] * a.K + (int64_t)b * kShrinkKB,
+               bytes, &bars[st]);
+  }
+
+  // All threads. The first min(nkb, nst) k-blocks must already be armed and
+  // issued. On return `out` is this lane's output: row warp*RPW + lane/BN,
+  // column lane % BN (not yet scaled). Returns false if a copy wait expired
+  // (after draining, bounded, every copy still in flight).
+  __device__ __forceinline__ bool run(const PartialArgs& a, float& out) const {
+    constexpr int RPW = G::RPW;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row0 = warp * RPW;
+    float2 acc[RPW][BN / 2];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+      for (int jp = 0; jp < BN / 2; ++jp) acc[rr][jp] = make_float2(0.0f, 0.0f);
+
+    int issued = min(nkb, nst);
+    int fail_b = -1;
+    for (int b = 0; b < nkb; ++b) {
+      const int st = b % nst;
+      const uint32_t parity = (uint32_t)((b / nst) & 1);
+      const bool ok = mbar_wait_bounded(&bars[st], parity, a.status);
+      if (__syncthreads_or(!ok)) { fail_b = b; break; }
+      const int64_t klen = min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB);
+      if ((int64_t)lane * 8 < klen && row0 < a.nrows) {
+        const uint8_t* sx = stages + st * kStageBytes;
+        const uint8_t* sa = sx + kTileRows * kRowBytes;
+        float2 xx[RPW][8];  // each x value duplicated into both halves
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+          float xv[8];
+          if (row0 + rr < a.nrows) {
+            const uint4 u = *reinterpret_cast<const uint4*>(sx + (row0 + rr) * kRowBytes + lane * 16);
+            unpack8(u, xv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) xx[rr][e] = make_float2(xv[e], xv[e]);
+        }
+#pragma unroll
+        for (int jp = 0; jp < BN / 2; ++jp) {
+          const uint4 u0 = *reinterpret_cast<const uint4*>(sa + (2 * jp) * kRowBytes + lane * 16);
+          const uint4 u1 = *reinterpret_cast<const uint4*>(sa + (2 * jp + 1) * kRowBytes + lane * 16);
+          float a0[8], a1[8];
+          unpack8(u0, a0);
+          unpack8(u1, a1);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 aa = make_float2(a0[e], a1[e]);
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) acc[rr][jp] = __ffma2_rn(xx[rr][e], aa, acc[rr][jp]);
+          }
+        }
+      }
+      __syncthreads();
+      if (b + nst < nkb) {
+        if (warp == 0) {
+          expect(a, b + nst);
+          issue_a(a, b + nst);
+          issue_x(a, b + nst);
+        }
+        issued = b + nst + 1;
+      }
+    }
+    if (fail_b >= 0) {
+      if (tid == 0)
+        for (int bb = fail_b; bb < issued; ++bb)
+          mbar_wait_bounded(&bars[bb % nst], (uint32_t)((bb / nst) & 1), a.status);
+      __syncthreads();
+      return false;
+    }
+
+    // Reduce-scatter: 32 values per lane (row-major rr*BN + j) -> one per lane.
+    float v[32];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+      for (int jp = 0; jp < BN / 2; ++jp) {
+        v[rr * BN + 2 * jp] = acc[rr][jp].x;
+        v[rr * BN + 2 * jp + 1] = acc[rr][jp].y;
+      }
+#pragma unroll
+    for (int lvl = 0; lvl < 5; ++lvl) {
+      const int off = 16 >> lvl;
+      const int half = 32 >> (lvl + 1);
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+        v[i] = keep + recv;
+      }
+    }
+    out = v[0];
+    return true;
+  }
+};
+
+}  // namespace ig

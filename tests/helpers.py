@@ -40,9 +40,9 @@ def shape_of(prob, mode=ig.MODE_DET, split_k=8, path=ig.PATH_AUTO, M=None):
 
 
 def run_apply(prob, mode=ig.MODE_DET, split_k=8, path=ig.PATH_AUTO, ws=None, z=None,
-              y=None, check=True):
+              y=None, check=True, shape=None):
     """lora_apply on copies of the problem's device tensors; returns (z, y)."""
-    sh = shape_of(prob, mode, split_k, path)
+    sh = shape_of(prob, mode, split_k, path) if shape is None else shape
     if ws is None:
         ws = ig.workspace(sh)
     if z is None:

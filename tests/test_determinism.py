@@ -166,8 +166,10 @@ def test_out_of_range_adapter_flagged():
 
 
 def test_poisoned_counters_detected_and_recovered():
+    # the counter protocol runs in the two-kernel path (lora_shrink, or
+    # lora_apply with IG_FLAG_UNFUSED)
     p = synth.make_problem(64, 4096, 256, 16, L=2, seed=4, device="cuda")
-    sh = shape_of(p)
+    sh = ig.make_shape(64, 4096, 256, 16, num_adapters=2, split_k=8, flags=ig.FLAG_UNFUSED)
     ws = ig.workspace(sh)
     ws[256:256 + 4 * 64].fill_(0x5A)        # garbage in the counter region
     z = torch.empty((1, 64, 16), dtype=torch.float32, device="cuda")
@@ -214,3 +216,137 @@ def test_workspace_reused_across_shapes_without_reinit():
         z, y = run_apply(p, mode=ig.MODE_DET, split_k=S, ws=ws)
         check_shrink(p.to("cpu"), z)
         check_expand(p.to("cpu"), z, y)
+
+
+@pytest.mark.parametrize("mode", [ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT],
+                         ids=["det", "atomic", "unsplit"])
+def test_dependent_layers_in_graph(mode):
+    """Kernels start early (programmatic dependent launch) but must not read
+    data the previous kernel writes before it has finished: chain layers so
+    that each layer's x is the previous layer's y, run the chain as one CUDA
+    graph with the static-weights flag, and compare with eager calls that
+    synchronise after every layer."""
+    M, K, L, r, layers = 48, 1024, 4, 16, 6
+    probs = [synth.make_problem(M, K, K, r, L=L, seed=700 + i, device="cuda")
+             for i in range(layers)]
+    idx = probs[0].idx
+    x0 = probs[0].x
+
+    def run(flags, graph):
+        sh = ig.make_shape(M, K, K, r, num_adapters=L, split_k=8, mode=mode, flags=flags)
+        ws = ig.workspace(sh)
+        ys = [p.y.clone() for p in probs]
+        zs = [torch.empty((1, M, r), dtype=torch.float32, device="cuda") for _ in probs]
+
+        def body(stream):
+            ig.map_tokens(sh, idx, ws, stream)
+            x = x0
+            for l, p in enumerate(probs):
+                ig.lora_apply(sh, x, ys[l], None, p.A, p.B, p.scale, zs[l], ws, stream)
+                if not graph:
+                    torch.cuda.synchronize()
+                x = ys[l]
+
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                body(s)                      # warm-up (also initialises state)
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            for l, p in enumerate(probs):
+                ys[l].copy_(p.y)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(torch.cuda.current_stream())
+            g.replay()
+            torch.cuda.synchronize()
+        else:
+            body(torch.cuda.current_stream())
+        assert ig.check_status(ws) == 0
+        return zs, ys
+
+    z_g, y_g = run(ig.FLAG_STATIC_WEIGHTS, graph=True)
+    if mode == ig.MODE_ATOMIC:
+        # no bitwise reference: check every layer against the oracle, with
+        # that layer's x being the previous layer's y from the same run
+        x = x0
+        for l, p in enumerate(probs):
+            q = synth.Problem(**{**p.__dict__, "x": x, "idx": idx})
+            check_shrink(q.to("cpu"), z_g[l])
+            check_expand(q.to("cpu"), z_g[l], y_g[l])
+            x = y_g[l]
+        return
+    z_e, y_e = run(0, graph=False)
+    for a, b in zip(y_e, y_g):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(z_e, z_g):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+FUSED_CASES = [
+    # M, K, N, r, slices, L, S, none_frac
+    (1, 4096, 4096, 16, 1, 8, 8, 0.0),
+    (8, 4096, 4096, 16, 1, 8, 8, 0.0),
+    (77, 4096, 264, 16, 3, 5, 8, 0.2),     # ragged columns per block, QKV slices
+    (256, 4096, 4096, 16, 1, 8, 8, 0.05),
+    (40, 512, 512, 8, 1, 1, 8, 0.0),
+    (33, 2048, 1024, 16, 1, 4, 1, 0.0),    # cluster of one
+    (33, 2048, 1024, 16, 1, 4, 2, 0.0),
+    (64, 8192, 1024, 16, 2, 4, 16, 0.1),   # 16-block clusters
+    (300, 11008, 4096, 8, 1, 6, 8, 0.0),   # K/S = 1376: ragged k-blocks
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "M%d_K%d_N%d_r%d_sl%d_S%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[6]))
+def test_fused_apply_bitwise_equals_two_kernels(case):
+    """lora_apply's one-launch cluster kernel (DET) and the two-kernel path
+    (Split-K shrink with the counter protocol, then expand) give the same bits
+    for z and y; and both are within tolerance of the oracle."""
+    M, K, N, r, slices, L, S, none_frac = case
+    p = synth.make_problem(M, K, N, r, slices=slices, L=L, seed=M + K + S,
+                           none_frac=none_frac, device="cuda")
+    outs = []
+    for flags in (0, ig.FLAG_UNFUSED, ig.FLAG_STATIC_WEIGHTS):
+        sh = ig.make_shape(M, K, N, r, slices=slices, num_adapters=L, split_k=S,
+                           mode=ig.MODE_DET, flags=flags)
+        if flags != ig.FLAG_UNFUSED:
+            assert ig.plan_query(sh)["apply_kernels"] == 1
+        z, y = run_apply(p, mode=ig.MODE_DET, split_k=S, ws=ig.workspace(sh),
+                         shape=sh)
+        outs.append((z, y))
+    for z, y in outs[1:]:
+        assert torch.equal(z.view(torch.int32), outs[0][0].view(torch.int32))
+        assert torch.equal(y.view(torch.int16), outs[0][1].view(torch.int16))
+    check_shrink(p.to("cpu"), outs[0][0])
+    check_expand(p.to("cpu"), outs[0][0], outs[0][1])
+
+
+@pytest.mark.parametrize("flags", [0, ig.FLAG_UNFUSED], ids=["fused", "two_kernel"])
+def test_batch_invariance_rank16(flags):
+    """Batch invariance of 64 probe rows at r = 16 (the fused kernel's rank)
+    over batch sizes 1..512."""
+    K, N, r, L = 4096, 1024, 16, 8
+    base = synth.make_problem(64, K, N, r, L=L, seed=2003, device="cuda")
+    sh0 = ig.make_shape(512, K, N, r, num_adapters=L, split_k=8, flags=flags)
+    ws = ig.workspace(sh0)
+    ref_z = ref_y = None
+    for b in range(1, 513):
+        x, y, idx, pos = synth.probe_batch(base.x, base.y, base.idx, b, L, seed=9000 + b,
+                                           device="cuda")
+        sh = ig.make_shape(b, K, N, r, num_adapters=L, split_k=8, flags=flags)
+        z = torch.empty((1, b, r), dtype=torch.float32, device="cuda")
+        ig.lora_apply(sh, x, y, idx, base.A, base.B, base.scale, z, ws)
+        pz = z[0, pos].view(torch.int32)
+        py = y[pos].view(torch.int16)
+        n = pos.numel()
+        if ref_z is None or n > ref_z.shape[0]:
+            if ref_z is not None:
+                assert torch.equal(pz[:ref_z.shape[0]], ref_z)
+                assert torch.equal(py[:ref_y.shape[0]], ref_y)
+            ref_z, ref_y = pz.clone(), py.clone()
+        else:
+            assert torch.equal(pz, ref_z[:n]), f"batch {b}"
+            assert torch.equal(py, ref_y[:n]), f"batch {b}"
+    assert ig.check_status(ws) == 0
