@@ -49,12 +49,13 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Plain (non-volatile) so that the S loads of one output can be in flight
+// together; the cluster barrier before them orders them after the writes.
 __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
   uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
   return v;
 }
 
@@ -189,8 +190,14 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
 
   // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
   for (int o = tid; o < nrows * BN; o += kThreads) {
+    float pv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (q < S) pv[q] = ld_dsmem_f32(part + o, (uint32_t)q);
     float total = 0.0f;
-    for (int q = 0; q < S; ++q) total += ld_dsmem_f32(part + o, (uint32_t)q);
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (q < S) total += pv[q];
     const float zv = total * p.scale;
     zs[o] = bf16_round_f32(zv);
     if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
@@ -199,28 +206,33 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
   __syncthreads();   // zs complete
 
   // Expand this block's columns: y = bf16_rn(f32(y) + sum_j zb_j B_nj), the
-  // j sum a chain of FMAs in increasing j (two columns per f32x2 FMA).
+  // j sum a chain of FMAs in increasing j (two columns per f32x2 FMA). Work
+  // units are (pair of rows, 8-column group), spread over all threads of
+  // the block; every element is computed by one thread, so the split does
+  // not change any result.
   const bool copies_ok = mbar_wait_bounded(bar_by, 0, p.status);
-  const int row0 = warp * RPW;
-  if (copies_ok && row0 < nrows) {
-    float2 zz[RPW][BN];  // this warp's Z rows, each value in both halves
+  const int pairs = (nrows + 1) / 2;
+  const int units = pairs * groups;
+  if (copies_ok) {
+    for (int u = tid; u < units; u += kThreads) {
+      const int rp = u / groups, q = u % groups;
+      const int ra = 2 * rp, rb = 2 * rp + 1;
+      const bool has_b = rb < nrows;
+      float2 acc[2][4];
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        const float zv = (row0 + rr < nrows) ? zs[(row0 + rr) * BN + j] : 0.0f;
-        zz[rr][j] = make_float2(zv, zv);
-      }
-    for (int q = lane; q < groups; q += 32) {  // this lane's 8-column group
-      float2 acc[RPW][4];
+        for (int cp = 0; cp < 4; ++cp) acc[i][cp] = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int rr = 0; rr < RPW; ++rr)
+      for (int h = 0; h < BN / 8; ++h) {
+        float za[8], zb[8];
 #pragma unroll
-        for (int cp = 0; cp < 4; ++cp) acc[rr][cp] = make_float2(0.0f, 0.0f);
+        for (int e = 0; e < 8; ++e) {
+          za[e] = zs[ra * BN + 8 * h + e];
+          zb[e] = has_b ? zs[rb * BN + 8 * h + e] : 0.0f;
+        }
 #pragma unroll
-      for (int cp = 0; cp < 4; ++cp) {
-#pragma unroll
-        for (int h = 0; h < BN / 8; ++h) {
+        for (int cp = 0; cp < 4; ++cp) {
           const uint4 u0 =
               *reinterpret_cast<const uint4*>(sB + q * lbs + ((2 * cp) * r + 8 * h) * 2);
           const uint4 u1 =
@@ -231,15 +243,14 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 bb = make_float2(b0[e], b1[e]);
-#pragma unroll
-            for (int rr = 0; rr < RPW; ++rr)
-              acc[rr][cp] = __ffma2_rn(zz[rr][8 * h + e], bb, acc[rr][cp]);
+            acc[0][cp] = __ffma2_rn(make_float2(za[e], za[e]), bb, acc[0][cp]);
+            acc[1][cp] = __ffma2_rn(make_float2(zb[e], zb[e]), bb, acc[1][cp]);
           }
         }
       }
 #pragma unroll
-      for (int rr = 0; rr < RPW; ++rr) {
-        const int row = row0 + rr;
+      for (int i = 0; i < 2; ++i) {
+        const int row = 2 * rp + i;
         if (row >= nrows) break;
         const uint4 yu = *reinterpret_cast<const uint4*>(sY + (row * ncols + q * 8) * 2);
         float yf[8];
@@ -247,8 +258,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
         uint32_t o[8];
 #pragma unroll
         for (int cp = 0; cp < 4; ++cp) {
-          o[2 * cp] = f32_to_bf16_bits(yf[2 * cp] + acc[rr][cp].x);
-          o[2 * cp + 1] = f32_to_bf16_bits(yf[2 * cp + 1] + acc[rr][cp].y);
+          o[2 * cp] = f32_to_bf16_bits(yf[2 * cp] + acc[i][cp].x);
+          o[2 * cp + 1] = f32_to_bf16_bits(yf[2 * cp + 1] + acc[i][cp].y);
         }
         uint4 w;
         w.x = o[0] | (o[1] << 16);
