@@ -118,6 +118,13 @@ int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
     if (e != cudaSuccess) return IG_ERR_CUDA;
   }
   ShrinkParams p;
+  int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
+                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IG_OK) return rc;
+  rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, kShrinkKB, (uint32_t)pl.bn,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IG_OK) return rc;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.A = static_cast<const __nv_bfloat16*>(A);
   p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
@@ -141,6 +148,14 @@ int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
 int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, const void* B,
               float scale, float* z, void* y, uint8_t* ws, cudaStream_t st) {
   FusedParams p;
+  // x rows are gathered 4 at a time (box 256 x 1); A blocks are r rows high
+  int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
+                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IG_OK) return rc;
+  rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, kShrinkKB, (uint32_t)sh->r,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IG_OK) return rc;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.A = static_cast<const __nv_bfloat16*>(A);
   p.B = static_cast<const __nv_bfloat16*>(B);

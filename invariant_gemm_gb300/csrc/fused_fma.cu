@@ -23,11 +23,11 @@
 //
 // Block = 16/RPW warps of RPW = 32/r rows; cluster = S blocks (rank s = K
 // partition s); tile = up to 16 token rows of one adapter (tile-table entry)
-// x all r rank columns (r = 8 or 16). Shared memory: the x/A ring of the shrink, the block's
-// partial, the tile's bf16-rounded Z, the block's B column slice (bulk
-// copies, padded for conflict-free reads) and the tile's y rows for those
-// columns (bulk copies, issued right after griddep_wait so they arrive while
-// the shrink computes).
+// x all r rank columns (r = 8 or 16). Copies: the A block of each k-block by
+// one tiled TMA copy, the token rows of x by row-gather TMA copies (4 rows
+// each), the block's B column slice (contiguous in B_stack) by one bulk copy;
+// the y values a thread will update are loaded into registers right after
+// griddep_wait, so they arrive while the shrink computes.
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -62,7 +62,12 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
 struct FusedLayout {
   int nst;           // ring depth
   int cols;          // output columns per block (multiple of 8)
-  size_t ring_off, part_off, zs_off, b_off, y_off, bytes;
+  size_t ring_off, part_off, zs_off, b_off, bytes;
+};
+
+template <int BN>
+struct ZsStride {
+  static constexpr int v = BN + 4;  // padded row: 8 rows hit 8 distinct bank groups
 };
 
 template <int BN>
@@ -74,14 +79,14 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   L.ring_off = 256;
   L.part_off = L.ring_off + (size_t)L.nst * PartialRing<BN>::kStageBytes;
   L.zs_off = L.part_off + kTileRows * BN * 4;
-  L.b_off = L.zs_off + kTileRows * BN * 4;
-  L.y_off = L.b_off + (size_t)(L.cols / 8) * (16 * BN + 16);
-  L.bytes = L.y_off + (size_t)kTileRows * L.cols * 2;
+  L.b_off = L.zs_off + kTileRows * ZsStride<BN>::v * 4;
+  L.bytes = L.b_off + (size_t)L.cols * BN * 2;
   return L;
 }
 
 template <int BN>
-__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(FusedParams p) {
+__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
+    fused_fma_kernel(const __grid_constant__ FusedParams p) {
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
   constexpr int RPW = ShrinkGeo<BN>::RPW;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -90,9 +95,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
   uint64_t* bar_by = bars + kShrinkStages;                       // B and y copies
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);        // tile entry
   float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [16][BN]
-  float* zs = reinterpret_cast<float*>(smem + lay.zs_off);       // [16][BN]
-  uint8_t* sB = smem + lay.b_off;
-  uint8_t* sY = smem + lay.y_off;
+  float* zs = reinterpret_cast<float*>(smem + lay.zs_off);       // [16][BN + 4]
+  uint8_t* sB = smem + lay.b_off;                                // [cols][BN] bf16
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
@@ -129,7 +133,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
   const int64_t c0 = (int64_t)s * lay.cols;
   const int ncols = (int)max((int64_t)0, min((int64_t)lay.cols, N - c0));
   const int groups = ncols / 8;
-  const int lbs = 16 * r + 16;
+  constexpr int ZS = ZsStride<BN>::v;
   const bool early_w = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
 
   PartialArgs pa;
@@ -140,6 +144,10 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
   pa.K = K;
   pa.Ks = p.Ks;
   pa.nrows = nrows;
+  pa.tm_x = &p.tm_x;
+  pa.tm_a = &p.tm_a;
+  pa.k0 = (int)((int64_t)s * p.Ks);
+  pa.a_row = (int)(((int64_t)g * p.slices + sl) * r);
   PartialRing<BN> ring;
   ring.stages = smem + lay.ring_off;
   ring.bars = bars;
@@ -148,27 +156,17 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
   const int first = min(ring.nkb, lay.nst);
 
   const __nv_bfloat16* Bsrc = p.B + (((int64_t)g * p.slices + sl) * N + c0) * r;
-  auto issue_b = [&]() {
-    for (int q = lane; q < groups; q += 32)
-      bulk_g2s(sB + q * lbs, Bsrc + (int64_t)q * 8 * r, 16 * r, bar_by);
-  };
+  const uint32_t b_bytes = (uint32_t)ncols * r * 2;
   const int64_t ldy = (int64_t)p.slices * N;
-  auto issue_y = [&]() {
-    if (ncols > 0)
-      for (int i = lane; i < nrows; i += 32)
-        bulk_g2s(sY + i * ncols * 2, p.y + (int64_t)rows_s[i] * ldy + (int64_t)sl * N + c0,
-                 (uint32_t)ncols * 2, bar_by);
-  };
 
   if (warp == 0) {
-    if (lane == 0)
-      mbar_arrive_expect_tx(bar_by, (uint32_t)groups * 16 * r + (uint32_t)nrows * ncols * 2);
+    if (lane == 0) mbar_arrive_expect_tx(bar_by, b_bytes);
     __syncwarp();
     for (int b = 0; b < first; ++b) {
       ring.expect(pa, b);
       if (early_w) ring.issue_a(pa, b);
     }
-    if (early_w) issue_b();
+    if (early_w && lane == 0 && b_bytes) bulk_g2s(sB, Bsrc, b_bytes, bar_by);
   }
   griddep_wait();
   griddep_launch();
@@ -177,8 +175,29 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
       if (!early_w) ring.issue_a(pa, b);
       ring.issue_x(pa, b);
     }
-    if (!early_w) issue_b();
-    issue_y();
+    if (!early_w && lane == 0 && b_bytes) bulk_g2s(sB, Bsrc, b_bytes, bar_by);
+  }
+
+  // Expand work units: (pair of rows rp, 8-column group q), rp varying
+  // fastest so that the 8 lanes of a shared-memory phase read the same B
+  // group (broadcast) and rows of Z that sit in distinct banks. The y values
+  // of a thread's first two units are loaded now and arrive during the
+  // shrink.
+  const int pairs = (nrows + 1) / 2;
+  const int units = pairs * groups;
+  uint4 ypre[2][2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int u = tid + k * kThreads;
+    if (u < units) {
+      const int rp = u % pairs, q = u / pairs;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int row = min(2 * rp + i, nrows - 1);
+        ypre[k][i] = *reinterpret_cast<const uint4*>(p.y + (int64_t)rows_s[row] * ldy +
+                                                     (int64_t)sl * N + c0 + q * 8);
+      }
+    }
   }
 
   float v;
@@ -199,7 +218,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
     for (int q = 0; q < 16; ++q)
       if (q < S) total += pv[q];
     const float zv = total * p.scale;
-    zs[o] = bf16_round_f32(zv);
+    zs[(o / BN) * ZS + o % BN] = bf16_round_f32(zv);
     if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
   }
   cluster_arrive();  // done reading the other blocks' partials
@@ -211,13 +230,25 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
   // the block; every element is computed by one thread, so the split does
   // not change any result.
   const bool copies_ok = mbar_wait_bounded(bar_by, 0, p.status);
-  const int pairs = (nrows + 1) / 2;
-  const int units = pairs * groups;
   if (copies_ok) {
-    for (int u = tid; u < units; u += kThreads) {
-      const int rp = u / groups, q = u % groups;
+    for (int k = 0; tid + k * kThreads < units; ++k) {
+      const int u = tid + k * kThreads;
+      const int rp = u % pairs, q = u / pairs;
       const int ra = 2 * rp, rb = 2 * rp + 1;
       const bool has_b = rb < nrows;
+      uint4 yv[2];
+      if (k == 0) {
+        yv[0] = ypre[0][0];
+        yv[1] = ypre[0][1];
+      } else if (k == 1) {
+        yv[0] = ypre[1][0];
+        yv[1] = ypre[1][1];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          yv[i] = *reinterpret_cast<const uint4*>(p.y + (int64_t)rows_s[min(ra + i, nrows - 1)] *
+                                                  ldy + (int64_t)sl * N + c0 + q * 8);
+      }
       float2 acc[2][4];
 #pragma unroll
       for (int i = 0; i < 2; ++i)
@@ -226,17 +257,23 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
 #pragma unroll
       for (int h = 0; h < BN / 8; ++h) {
         float za[8], zb[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          za[e] = zs[ra * BN + 8 * h + e];
-          zb[e] = has_b ? zs[rb * BN + 8 * h + e] : 0.0f;
+        {
+          const float4 a0 = *reinterpret_cast<const float4*>(zs + ra * ZS + 8 * h);
+          const float4 a1 = *reinterpret_cast<const float4*>(zs + ra * ZS + 8 * h + 4);
+          const float4 b0 = *reinterpret_cast<const float4*>(zs + (has_b ? rb : ra) * ZS + 8 * h);
+          const float4 b1 =
+              *reinterpret_cast<const float4*>(zs + (has_b ? rb : ra) * ZS + 8 * h + 4);
+          za[0] = a0.x; za[1] = a0.y; za[2] = a0.z; za[3] = a0.w;
+          za[4] = a1.x; za[5] = a1.y; za[6] = a1.z; za[7] = a1.w;
+          zb[0] = b0.x; zb[1] = b0.y; zb[2] = b0.z; zb[3] = b0.w;
+          zb[4] = b1.x; zb[5] = b1.y; zb[6] = b1.z; zb[7] = b1.w;
         }
 #pragma unroll
         for (int cp = 0; cp < 4; ++cp) {
           const uint4 u0 =
-              *reinterpret_cast<const uint4*>(sB + q * lbs + ((2 * cp) * r + 8 * h) * 2);
+              *reinterpret_cast<const uint4*>(sB + ((q * 8 + 2 * cp) * r + 8 * h) * 2);
           const uint4 u1 =
-              *reinterpret_cast<const uint4*>(sB + q * lbs + ((2 * cp + 1) * r + 8 * h) * 2);
+              *reinterpret_cast<const uint4*>(sB + ((q * 8 + 2 * cp + 1) * r + 8 * h) * 2);
           float b0[8], b1[8];
           unpack8(u0, b0);
           unpack8(u1, b1);
@@ -250,11 +287,10 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) fused_fma_kernel(Fused
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int row = 2 * rp + i;
+        const int row = ra + i;
         if (row >= nrows) break;
-        const uint4 yu = *reinterpret_cast<const uint4*>(sY + (row * ncols + q * 8) * 2);
         float yf[8];
-        unpack8(yu, yf);
+        unpack8(yv[i], yf);
         uint32_t o[8];
 #pragma unroll
         for (int cp = 0; cp < 4; ++cp) {

@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -74,6 +75,8 @@ struct MapParams {
 };
 
 struct ShrinkParams {
+  CUtensorMap tm_x;     // x [M][K], box 256 x 1 (row gathers)
+  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 256 x BN
   const __nv_bfloat16* x;
   const __nv_bfloat16* A;
   const int32_t* tiles;
@@ -96,7 +99,15 @@ struct ExpandParams {
   int32_t slices, L, ntiles, flags;
 };
 
+// 2-D bf16 tensor map [rows][cols] with the given row stride; box
+// box_cols x box_rows; swizzle is a CUtensorMapSwizzle value. IG_OK or
+// IG_ERR_CUDA (driver entry point missing or encode rejected).
+int encode_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows, int swizzle);
+
 struct FusedParams {
+  CUtensorMap tm_x;     // x [M][K], box 256 x 1 (row gathers)
+  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 256 x r
   const __nv_bfloat16* x;
   const __nv_bfloat16* A;
   const __nv_bfloat16* B;
@@ -210,6 +221,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
   }
   return true;
+}
+
+// Tiled 2-D tensor copy global -> shared (box of the tensor map at
+// coordinates {c0 = column, c1 = row}); c0 * 2 bytes must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+        "r"(smem_u32(bar)) : "memory");
+}
+// Row gather: four rows r0..r3 of a 2-D tensor map whose box is one row high,
+// columns [c0, c0 + box), written one after the other to dst.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1),
+        "r"(r2), "r"(r3), "r"(smem_u32(bar)) : "memory");
 }
 
 // One-dimensional bulk copy global -> shared, completion counted in bytes on

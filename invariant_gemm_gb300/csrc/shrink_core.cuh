@@ -5,9 +5,12 @@
 // Tile: up to 16 token rows x BN rank columns (BN = 8 or 16). The block has
 // 16/RPW warps of RPW = 32/BN rows each, so every lane ends with exactly one
 // finished output. The partition [k0, k0 + Ks) is streamed through a ring of
-// `nst` shared-memory stages, k-blocks of 256 elements, by 1-D bulk async
-// copies: one per token row (x) and one per rank column (A), completion
-// counted in bytes on one mbarrier per stage. Warp 0 issues the copies.
+// `nst` shared-memory stages, k-blocks of 256 elements, completion counted in
+// bytes on one mbarrier per stage; warp 0 issues the copies. Two ways to
+// copy: with tensor maps, one tiled TMA copy brings the A block (BN rows)
+// and one row-gather TMA copy per 4 token rows brings x (boxes are always
+// 256 wide; columns past the partition are loaded but not used); without,
+// one 1-D bulk copy per row.
 //
 // Order of the sum, identical for every row and every M ("Reproducible LoRA
 // Inference Through Deterministic Split-K Reduction" leaves the order inside
@@ -39,6 +42,11 @@ struct PartialArgs {
   int64_t K;                  // row stride of x and A, in elements
   int64_t Ks;                 // partition length
   int nrows;
+  // tensor-map copies (both null: 1-D bulk copies)
+  const CUtensorMap* tm_x;    // x [M][K], box 256 x 1
+  const CUtensorMap* tm_a;    // A as [rows][K], box 256 x BN
+  int k0;                     // partition start (column coordinate)
+  int a_row;                  // row coordinate of the tile's first A row
 };
 
 template <int BN>
@@ -56,15 +64,21 @@ struct PartialRing {
   }
   // warp 0: arm stage b % nst for all copies of k-block b
   __device__ __forceinline__ void expect(const PartialArgs& a, int b) const {
-    if ((threadIdx.x & 31) == 0)
-      mbar_arrive_expect_tx(&bars[b % nst], block_bytes(a, b) * (uint32_t)(a.nrows + BN));
+    uint32_t bytes;
+    if (a.tm_x) bytes = (uint32_t)kRowBytes * (BN + 4 * ((a.nrows + 3) / 4));
+    else bytes = block_bytes(a, b) * (uint32_t)(a.nrows + BN);
+    if ((threadIdx.x & 31) == 0) mbar_arrive_expect_tx(&bars[b % nst], bytes);
     __syncwarp();
   }
   __device__ __forceinline__ void issue_a(const PartialArgs& a, int b) const {
     const int lane = threadIdx.x & 31;
     const int st = b % nst;
-    const uint32_t bytes = block_bytes(a, b);
     uint8_t* sa = stages + st * kStageBytes + kTileRows * kRowBytes;
+    if (a.tm_a) {
+      if (lane == 0) tma_load_2d(sa, a.tm_a, a.k0 + b * kShrinkKB, a.a_row, &bars[st]);
+      return;
+    }
+    const uint32_t bytes = block_bytes(a, b);
     for (int j = lane; j < BN; j += 32)
       bulk_g2s(sa + j * kRowBytes, a.A + (int64_t)j * a.K + (int64_t)b * kShrinkKB, bytes,
                &bars[st]);
@@ -72,8 +86,18 @@ struct PartialRing {
   __device__ __forceinline__ void issue_x(const PartialArgs& a, int b) const {
     const int lane = threadIdx.x & 31;
     const int st = b % nst;
-    const uint32_t bytes = block_bytes(a, b);
     uint8_t* sx = stages + st * kStageBytes;
+    if (a.tm_x) {
+      // rows past nrows repeat the last row: loaded, never used
+      if (4 * lane < a.nrows) {
+        const int last = a.nrows - 1;
+        tma_gather4(sx + 4 * lane * kRowBytes, a.tm_x, a.k0 + b * kShrinkKB,
+                    a.rows[min(4 * lane, last)], a.rows[min(4 * lane + 1, last)],
+                    a.rows[min(4 * lane + 2, last)], a.rows[min(4 * lane + 3, last)], &bars[st]);
+      }
+      return;
+    }
+    const uint32_t bytes = block_bytes(a, b);
     for (int i = lane; i < a.nrows; i += 32)
       bulk_g2s(sx + i * kRowBytes, a.x + (int64_t)a.rows[i] * a.K + (int64_t)b * kShrinkKB,
                bytes, &bars[st]);

@@ -14,9 +14,9 @@
 // Block = 16/RPW warps of RPW = 32/BN rows (8 x 2 for BN = 16, 4 x 4 for
 // BN = 8), tile = up to 16 token rows of one adapter (one entry of the token
 // map's tile table) x BN rank columns, one K partition. The partition
-// is streamed through shared memory in k-blocks of 256 elements by 1-D bulk
-// async copies (one per token row and one per A row, completion counted on
-// an mbarrier), four stages deep.
+// is streamed through shared memory in k-blocks of 256 elements by TMA
+// copies (one tiled copy for the A block, one row gather per 4 token rows,
+// completion counted on an mbarrier), four stages deep.
 //
 // Latency: the tile entry is read before griddep_wait() (the token map is
 // complete before this kernel starts); with IG_FLAG_STATIC_WEIGHTS the A
@@ -42,7 +42,8 @@ struct ShrinkSmem {
 };
 
 template <int BN, int MODE>
-__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) shrink_fma_kernel(ShrinkParams p) {
+__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
+    shrink_fma_kernel(const __grid_constant__ ShrinkParams p) {
   using SM = ShrinkSmem<BN>;
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
   constexpr int RPW = ShrinkGeo<BN>::RPW;
@@ -101,6 +102,10 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS) shrink_fma_kernel(Shri
   pa.K = K;
   pa.Ks = p.Ks;
   pa.nrows = nrows;
+  pa.tm_x = &p.tm_x;
+  pa.tm_a = &p.tm_a;
+  pa.k0 = (int)k0;
+  pa.a_row = (int)(((int64_t)g * p.slices + sl) * r + (int64_t)jb * BN);
   PartialRing<BN> ring;
   ring.stages = stages;
   ring.bars = bars;
