@@ -17,6 +17,7 @@ struct Plan {
   int64_t Ks;        // K / S
   int bn;            // shrink rank columns per tile
   int jblocks;       // r / bn
+  int tile_rows;     // rows per tile: 16 (CUDA cores) or 128 (tensor cores)
   int64_t tiles;     // tile-table entries: upper bound on tiles (groups 0..L)
   int ntiles;        // expand column tiles per slice
   size_t off_perm, off_offsets, off_tiles, off_partials, total;
@@ -48,17 +49,24 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   int S = sh->mode == IG_MODE_UNSPLIT ? 1 : sh->split_k;
   if (S < 1) return IG_ERR_SHAPE;
   if ((K / 8) % S) return IG_ERR_SHAPE;
-  int path = sh->path == IG_PATH_AUTO ? IG_PATH_FMA : sh->path;
-  if (path == IG_PATH_MMA) return IG_ERR_UNSUPPORTED;
+  // Tensor cores where the token x rank x K tile is a dense contraction:
+  // ranks of 32 and more (prefill-class adapters). Decided from r and K/S,
+  // never from M.
+  const bool mma_ok = r % 16 == 0 && (K / S) % 16 == 0 && r <= 256;
+  int path = sh->path;
+  if (path == IG_PATH_AUTO) path = (mma_ok && r >= 32) ? IG_PATH_MMA : IG_PATH_FMA;
+  if (path == IG_PATH_MMA && !mma_ok) return IG_ERR_UNSUPPORTED;
 
   pl->path = path;
   pl->mode = sh->mode;
   pl->S = S;
   pl->Ks = K / S;
-  pl->bn = (r % 16 == 0) ? 16 : 8;
-  pl->jblocks = (int)(r / pl->bn);
+  const bool mma = path == IG_PATH_MMA;
+  pl->bn = mma ? (int)r : ((r % 16 == 0) ? 16 : 8);
+  pl->jblocks = mma ? 1 : (int)(r / pl->bn);
+  pl->tile_rows = mma ? kMmaTileRows : kTileRows;
   const int L = sh->num_adapters;
-  pl->tiles = tiles_upper_bound(M, L + 1, kTileRows);
+  pl->tiles = tiles_upper_bound(M, L + 1, pl->tile_rows);
   pl->ntiles = (int)((N + kExpandBN - 1) / kExpandBN);
   const int64_t slots = pl->tiles * sh->slices * pl->jblocks;
   if (sh->mode == IG_MODE_DET && slots > kMaxCounters) return IG_ERR_UNSUPPORTED;
@@ -66,9 +74,11 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   pl->off_perm = kMapOffset;
   pl->off_offsets = align_up(pl->off_perm + 4 * (size_t)M, 256);
   pl->off_tiles = align_up(pl->off_offsets + 4 * (size_t)(L + 2), 256);
-  pl->off_partials = align_up(pl->off_tiles + 4 * (size_t)kTileInts * pl->tiles, 256);
+  pl->off_partials =
+      align_up(pl->off_tiles + 4 * (size_t)(4 + pl->tile_rows) * pl->tiles, 256);
   size_t part = 0;
-  if (sh->mode == IG_MODE_DET) part = (size_t)slots * S * kTileRows * pl->bn * sizeof(float);
+  if (sh->mode == IG_MODE_DET)
+    part = (size_t)slots * S * pl->tile_rows * pl->bn * sizeof(float);
   pl->total = align_up(pl->off_partials + part, 256);
 
   pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_FMA && (r == 8 || r == 16) &&
@@ -77,7 +87,7 @@ int make_plan(const ig_shape* sh, Plan* pl) {
 
   uint64_t h = 1469598103934665603ull;
   const int64_t fields[] = {IG_ABI_VERSION, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
-                            pl->bn, kShrinkKB};
+                            pl->bn, mma ? 64 : kShrinkKB};
   for (int64_t f : fields) h = fnv1a(h, f);
   pl->key = h;
   return IG_OK;
@@ -107,8 +117,60 @@ int run_map(const ig_shape* sh, const Plan& pl, const int32_t* idx, uint8_t* ws,
   mp.status = reinterpret_cast<uint32_t*>(ws);
   mp.M = sh->M;
   mp.tiles_max = pl.tiles;
+  mp.tile_rows = pl.tile_rows;
   mp.L = sh->num_adapters;
   return cuda_status(launch_map_tokens(mp, st));
+}
+
+int run_shrink_mma(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
+                   float scale, float* z, uint8_t* ws, cudaStream_t st) {
+  MmaShrinkParams p;
+  int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
+                         1, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
+  rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)sh->r,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
+  p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
+  p.z = z;
+  p.partials = reinterpret_cast<float*>(ws + pl.off_partials);
+  p.counters = reinterpret_cast<uint32_t*>(ws + kCountersOffset);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.M = sh->M;
+  p.K = sh->K;
+  p.r = sh->r;
+  p.Ks = pl.Ks;
+  p.slices = sh->slices;
+  p.L = sh->num_adapters;
+  p.S = pl.S;
+  p.flags = sh->flags;
+  p.scale = scale;
+  return cuda_status(launch_shrink_mma(p, pl.mode, pl.tiles, st));
+}
+
+int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
+                   uint8_t* ws, cudaStream_t st) {
+  MmaExpandParams p;
+  int rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N,
+                         (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, 256,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
+  rc = encode_map_2d(&p.tm_y, y, (uint64_t)sh->M, (uint64_t)sh->slices * sh->N,
+                     (uint64_t)sh->slices * sh->N * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
+  p.z = z;
+  p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.M = sh->M;
+  p.N = sh->N;
+  p.r = sh->r;
+  p.slices = sh->slices;
+  p.L = sh->num_adapters;
+  p.ntiles = pl.ntiles;
+  p.flags = sh->flags;
+  return cuda_status(launch_expand_mma(p, pl.tiles, st));
 }
 
 int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A, float scale,
@@ -117,6 +179,7 @@ int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
     cudaError_t e = cudaMemsetAsync(z, 0, sizeof(float) * sh->slices * sh->M * sh->r, st);
     if (e != cudaSuccess) return IG_ERR_CUDA;
   }
+  if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st);
   ShrinkParams p;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
                          kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -177,6 +240,7 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
 
 int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
                uint8_t* ws, cudaStream_t st) {
+  if (pl.path == IG_PATH_MMA) return run_expand_mma(sh, pl, z, B, y, ws, st);
   ExpandParams p;
   p.z = z;
   p.B = static_cast<const __nv_bfloat16*>(B);
@@ -233,9 +297,9 @@ int ig_plan_query(const ig_shape* shape, ig_plan_info* out) {
   out->path = pl.path;
   out->split_k = pl.S;
   out->k_split = pl.Ks;
-  out->shrink_bm = kTileRows;
+  out->shrink_bm = pl.tile_rows;
   out->shrink_bn = pl.bn;
-  out->expand_bm = kExpandBM;
+  out->expand_bm = pl.tile_rows;
   out->expand_bn = kExpandBN;
   out->shrink_tiles_max = pl.tiles;
   out->shrink_ctas_max = pl.tiles * shape->slices * pl.jblocks * pl.S;

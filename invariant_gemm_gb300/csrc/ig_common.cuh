@@ -54,6 +54,9 @@ constexpr int kExpandBM = kExpandWarps * kExpandRowsPerWarp;  // 16 = kTileRows
 constexpr int kExpandBN = 256;        // output columns: 32 lanes x 8
 constexpr int kExpandJC = 16;         // rank elements per register chunk
 static_assert(kExpandBM == kTileRows, "tile rows");
+// tensor-core path: 128-row tiles (the MMA's M)
+constexpr int kMmaTileRows = 128;
+constexpr int kMmaTileInts = 4 + kMmaTileRows;
 
 // Tile count over token groups: sum over groups g of ceil(count_g / bm),
 // bounded by floor(M / bm) + (number of non-empty groups).
@@ -72,6 +75,7 @@ struct MapParams {
   int64_t M;
   int64_t tiles_max;
   int32_t L;
+  int32_t tile_rows;   // 16 (CUDA-core path) or 128 (tensor-core path)
 };
 
 struct ShrinkParams {
@@ -120,6 +124,30 @@ struct FusedParams {
   float scale;
 };
 
+struct MmaShrinkParams {
+  CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
+  const int32_t* tiles; // 128-row tile table
+  float* z;
+  float* partials;
+  uint32_t* counters;
+  uint32_t* status;
+  int64_t M, K, r, Ks;
+  int32_t slices, L, S, flags;
+  float scale;
+};
+
+struct MmaExpandParams {
+  CUtensorMap tm_b;     // B_stack as [L*slices*N][r], box 64 x 256, 128-byte swizzle
+  CUtensorMap tm_y;     // y [M][slices*N], box 64 x 1, 128-byte swizzle (row gathers)
+  const float* z;
+  const int32_t* tiles; // 128-row tile table
+  __nv_bfloat16* y;
+  uint32_t* status;
+  int64_t M, N, r;
+  int32_t slices, L, ntiles, flags;
+};
+
 // Launchers (defined in the .cu files); they return cudaGetLastError().
 cudaError_t launch_map_tokens(const MapParams& p, cudaStream_t st);
 cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn,
@@ -128,6 +156,10 @@ cudaError_t launch_expand_fma(const ExpandParams& p, int64_t tiles_max,
                               cudaStream_t st);
 cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st);
 size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S);
+cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
+                              cudaStream_t st);
+cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st);
+size_t expand_mma_smem_bytes(int r);
 
 // Launch helper: programmatic dependent launch on `st` (see griddep_wait).
 template <typename Kern, typename P>

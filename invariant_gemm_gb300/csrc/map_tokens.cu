@@ -18,9 +18,10 @@
 // start[warp][g] + (rank among equal groups within the 32-row step).
 //
 // Finally it writes the tile table the shrink and expand kernels read: group
-// g is cut into ceil(count_g / 16) tiles of at most 16 consecutive rows of
-// the grouped order; tile entries hold [g, nrows, 0, 0, rows[16]] so that a
-// block learns its adapter and its token rows with one 80-byte load. Tiles of
+// g is cut into ceil(count_g / T) tiles of at most T consecutive rows of the
+// grouped order (T = 16 for the CUDA-core kernels, 128 for the tensor-core
+// ones); tile entries hold [g, nrows, 0, 0, rows[T]] so that a block learns
+// its adapter and its token rows with one contiguous load. Tiles of
 // adapters 0..L-1 come first (in adapter order), then the no-adapter group,
 // then empty entries (nrows = 0) up to tiles_max.
 //
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
     int32_t carry = 0;
     for (int base = 0; base < G; base += 32) {
       const int g = base + lane;
-      const int32_t c = g < G ? (cntg[g] + kTileRows - 1) / kTileRows : 0;
+      const int32_t c = g < G ? (cntg[g] + p.tile_rows - 1) / p.tile_rows : 0;
       int32_t incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -151,12 +152,14 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
   }
   __syncthreads();
 
-  // tile table: one warp per tile, lane i < 16 writes row i
+  // tile table: one warp per tile
+  const int T = p.tile_rows;
+  const int ents = 4 + T;
   const int64_t ntiles = tstart[G];
   for (int64_t t = warp; t < p.tiles_max; t += kMapWarps) {
-    int32_t* ent = p.tiles + t * kTileInts;
+    int32_t* ent = p.tiles + t * ents;
     if (t >= ntiles) {
-      if (lane < kTileInts) ent[lane] = lane == 0 ? -1 : 0;
+      for (int i = lane; i < ents; i += 32) ent[i] = i == 0 ? -1 : 0;
       continue;
     }
     int lo_g = 0, hi_g = G - 1;  // last group with tstart[g] <= t
@@ -166,12 +169,12 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
     }
     const int g = lo_g;
     const int q = (int)(t - tstart[g]);
-    const int first = total[g] + q * kTileRows;          // total[] holds group starts
-    const int cnt = min(kTileRows, total[g] + cntg[g] - first);
+    const int first = total[g] + q * T;                   // total[] holds group starts
+    const int cnt = min(T, total[g] + cntg[g] - first);
     if (lane == 0) ent[0] = g;
     if (lane == 1) ent[1] = cnt;
     if (lane == 2 || lane == 3) ent[lane] = 0;
-    if (lane < kTileRows) ent[4 + lane] = lane < cnt ? p.perm[first + lane] : 0;
+    for (int i = lane; i < T; i += 32) ent[4 + i] = i < cnt ? p.perm[first + i] : 0;
   }
 }
 

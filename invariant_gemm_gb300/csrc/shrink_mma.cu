@@ -1,0 +1,283 @@
+// LoRA shrink on the tcgen05 tensor cores: Z = scale * X A_i^T with a Split-K
+// reduction, for ranks where the token x rank x K tile is a real dense
+// contraction (prefill).
+//
+// "Reproducible LoRA Inference Through Deterministic Split-K Reduction":
+//   Eq. 3 / Fig. 1  S thread blocks per output tile, block s over the s-th
+//                   contiguous K partition;
+//   Algorithm 1     DET: FP32 partial -> scratch, gpu fence, block barrier,
+//                   acq_rel integer increment of the tile's counter; the block
+//                   that saw S-1 sums scratch[t][0..S-1] in increasing order,
+//                   multiplies by the scale, writes the tile, zeroes the
+//                   counter;
+//   sec. 4.1        ATOMIC: FP32 atomic add of scale * partial into zeroed Z;
+//   sec. 4.2        UNSPLIT: S = 1.
+//
+// Block = 4 warps, tile = up to 128 token rows of one adapter (one entry of
+// the token map's 128-row tile table) x all r rank columns. One thread of
+// warp 0 issues the TMA copies: per k-step of 64 elements, row gathers of x
+// (4 rows each, only the tile's rows) and one tiled copy of the A block
+// (r rows), both 128-byte swizzled, into a 4-deep ring. One thread of warp 1
+// issues per k-step four tcgen05.mma (M = 128 tokens, N = r, K = 16) into an
+// FP32 accumulator in tensor memory and commits each stage back to the
+// producer. The last k-step of a partition that is not a multiple of 64
+// issues only the MMAs inside the partition. All 4 warps then read the
+// accumulator (warp w: token rows 32w .. 32w+31, one row per thread).
+//
+// Arithmetic order, fixed by K/S and r only: the tensor core's FP32
+// accumulation of the K-steps in order within the partition, then the
+// partitions summed in increasing order. A row's value depends only on that
+// row, its adapter and the plan.
+#include "umma.cuh"
+
+namespace ig {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kStages = 4;
+constexpr int kKStep = 64;                      // elements per k-step (128 bytes)
+constexpr int kXTileBytes = kMmaTileRows * 128;  // 16 KB
+
+struct Ctl {                       // control block at the start of shared memory
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t done;
+  uint32_t tmem;
+  int32_t info[4];
+};
+
+__host__ __device__ inline size_t mma_shrink_smem(int r) {
+  const size_t stage = kXTileBytes + (size_t)r * 128;
+  return 1024 /*align slack*/ + 1024 /*ctl*/ + (size_t)kMmaTileInts * 4 + kStages * stage + 1024;
+}
+
+__host__ __device__ inline uint32_t tmem_cols_for(int r) {
+  uint32_t c = 32;
+  while (c < (uint32_t)r) c <<= 1;
+  return c;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+    shrink_mma_kernel(const __grid_constant__ MmaShrinkParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned working area (128-byte swizzle atoms)
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem);
+  int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 1024);
+  uint8_t* ring = smem + 1024 + ((kMmaTileInts * 4 + 1023) / 1024) * 1024;
+  const int r = (int)p.r;
+  const int stage_bytes = kXTileBytes + r * 128;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.S;
+  int64_t bid = blockIdx.x;
+  const int s = (int)(bid % S);
+  bid /= S;
+  const int sl = (int)(bid % p.slices);
+  const int64_t t = bid / p.slices;
+
+  for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], 1);
+    }
+    mbar_init(&ctl->done, 1);
+    fence_mbar_init();
+  }
+  const uint32_t ncols = tmem_cols_for(r);
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  const int g = ent_s[0];
+  const int nrows = ent_s[1];
+  const int32_t* rows_s = ent_s + 4;
+  const int64_t M = p.M;
+
+  auto teardown = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, ncols);
+  };
+
+  if (nrows <= 0) {
+    teardown();
+    return;
+  }
+  if (g == p.L) {
+    griddep_wait();
+    griddep_launch();
+    if (MODE != IG_MODE_ATOMIC && s == 0)
+      for (int i = tid; i < nrows * r; i += kThreads)
+        p.z[((int64_t)sl * M + rows_s[i / r]) * r + i % r] = 0.0f;
+    teardown();
+    return;
+  }
+
+  const int64_t Ks = p.Ks;
+  const int k0 = (int)((int64_t)s * Ks);
+  const int nk = (int)((Ks + kKStep - 1) / kKStep);      // k-steps
+  const int a_row = (int)(((int64_t)g * p.slices + sl) * r);
+  const int groups4 = (nrows + 3) / 4;
+  const uint32_t stage_tx = (uint32_t)groups4 * 4 * 128 + (uint32_t)r * 128;
+  const bool early_a = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
+  const int first = min(nk, kStages);
+
+  auto issue_a = [&](int b) {
+    uint8_t* st = ring + (b % kStages) * stage_bytes;
+    tma_load_2d(st + kXTileBytes, &p.tm_a, k0 + b * kKStep, a_row, &ctl->full[b % kStages]);
+  };
+  auto issue_x = [&](int b) {
+    uint8_t* st = ring + (b % kStages) * stage_bytes;
+    const int last = nrows - 1;
+    for (int q = 0; q < groups4; ++q)
+      tma_gather4(st + q * 4 * 128, &p.tm_x, k0 + b * kKStep, rows_s[min(4 * q, last)],
+                  rows_s[min(4 * q + 1, last)], rows_s[min(4 * q + 2, last)],
+                  rows_s[min(4 * q + 3, last)], &ctl->full[b % kStages]);
+  };
+
+  bool failed = false;
+  if (warp == 0 && lane == 0) {
+    for (int b = 0; b < first; ++b) {
+      mbar_arrive_expect_tx(&ctl->full[b], stage_tx);
+      if (early_a) issue_a(b);
+    }
+  }
+  griddep_wait();
+  griddep_launch();
+
+  if (warp == 0 && lane == 0) {
+    // producer
+    for (int b = 0; b < nk; ++b) {
+      if (b >= first) {
+        const int st = b % kStages;
+        if (!mbar_wait_bounded(&ctl->empty[st], (uint32_t)(((b / kStages) - 1) & 1), p.status)) {
+          failed = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&ctl->full[st], stage_tx);
+        issue_a(b);
+      } else if (!early_a) {
+        issue_a(b);
+      }
+      issue_x(b);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, r);
+    for (int b = 0; b < nk; ++b) {
+      const int st = b % kStages;
+      if (!mbar_wait_bounded(&ctl->full[st], (uint32_t)((b / kStages) & 1), p.status)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t xs = smem_u32(ring + st * stage_bytes);
+      const uint32_t as = xs + kXTileBytes;
+      const int64_t rem = Ks - (int64_t)b * kKStep;
+      const int ksub = (int)min((int64_t)4, (rem + 15) / 16);
+      for (int kk = 0; kk < ksub; ++kk)
+        umma_bf16(tmem, umma_desc_sw128(xs + kk * 32), umma_desc_sw128(as + kk * 32), idesc,
+                  b > 0 || kk > 0);
+      umma_commit(&ctl->empty[st]);
+    }
+    umma_commit(&ctl->done);  // also after a failure: tracks everything issued
+  }
+  __syncwarp();
+
+  // epilogue: wait for the accumulator
+  const bool acc_ok = mbar_wait_bounded(&ctl->done, 0, p.status);
+  tc_fence_after();
+  const int row = warp * 32 + lane;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const int64_t slot = t * p.slices + sl;
+  float* part = p.partials + slot * (int64_t)S * (kMmaTileRows * r);
+  for (int c = 0; c < r; c += 32) {
+    float v[32];
+    tmem_ld32(trow + c, v);
+    if (!acc_ok || row >= nrows) continue;
+    const int nv = min(32, r - c);   // r is a multiple of 16
+    if (MODE == IG_MODE_DET) {
+      float4* dst = reinterpret_cast<float4*>(part + (int64_t)s * (kMmaTileRows * r) +
+                                              (int64_t)row * r + c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (4 * i < nv) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+      float* zp = p.z + ((int64_t)sl * M + rows_s[row]) * r + c;
+      if (MODE == IG_MODE_UNSPLIT) {
+        float4* z4 = reinterpret_cast<float4*>(zp);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (4 * i < nv)
+            z4[i] = make_float4(v[4 * i] * p.scale, v[4 * i + 1] * p.scale,
+                                v[4 * i + 2] * p.scale, v[4 * i + 3] * p.scale);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nv) atomicAdd(zp + i, v[i] * p.scale);
+      }
+    }
+  }
+
+  if (MODE == IG_MODE_DET) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t prev = atom_add_acq_rel_gpu(p.counters + slot, 1u);
+      ctl->info[0] = (int)prev;
+      if (prev >= (uint32_t)S) atomicOr(p.status, kStatusCorrupt);
+    }
+    __syncthreads();
+    if ((uint32_t)ctl->info[0] == (uint32_t)(S - 1)) {
+      __threadfence();
+      for (int o = tid; o < nrows * r; o += kThreads) {
+        float total = 0.0f;
+        for (int q = 0; q < S; ++q)
+          total += __ldcg(part + (int64_t)q * (kMmaTileRows * r) + o);
+        p.z[((int64_t)sl * M + rows_s[o / r]) * r + o % r] = total * p.scale;
+      }
+      if (tid == 0) p.counters[slot] = 0u;
+    }
+  }
+
+  if (failed || !acc_ok) {
+    // drain (bounded) the copies of stages that were issued and not consumed
+    if (tid == 0)
+      for (int st = 0; st < kStages; ++st)
+        mbar_wait_bounded(&ctl->full[st], 0, p.status);
+  }
+  teardown();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
+  auto kern = shrink_mma_kernel<MODE>;
+  const size_t smem = mma_shrink_smem((int)p.r);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = tiles_max * p.slices * p.S;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
+}
+
+}  // namespace
+
+cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
+                              cudaStream_t st) {
+  if (mode == IG_MODE_DET) return launch_mode<IG_MODE_DET>(p, tiles_max, st);
+  if (mode == IG_MODE_ATOMIC) return launch_mode<IG_MODE_ATOMIC>(p, tiles_max, st);
+  return launch_mode<IG_MODE_UNSPLIT>(p, tiles_max, st);
+}
+
+}  // namespace ig

@@ -1,0 +1,80 @@
+"""The tcgen05 tensor-core path (ranks of 32 and more by default, or forced
+with PATH_MMA) against the FP64 oracle: bit-exact on small-integer inputs
+(products exact, sums below 2^24), within tolerance on normal inputs, every
+mode, ragged partitions (K/S not a multiple of 64), partial tiles, no-adapter
+rows, several slices, and the plan's path choice."""
+import numpy as np
+import pytest
+import torch
+
+import invariant_gemm_gb300 as ig
+import synth
+from helpers import check_expand, check_shrink, need_gpu, run_apply
+
+pytestmark = pytest.mark.gpu
+
+MODES = [ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT]
+MODE_ID = {ig.MODE_DET: "det", ig.MODE_ATOMIC: "atomic", ig.MODE_UNSPLIT: "unsplit"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def test_plan_picks_tensor_cores_for_large_ranks():
+    for r, want in [(16, ig.PATH_FMA), (24, ig.PATH_FMA), (32, ig.PATH_MMA), (64, ig.PATH_MMA),
+                    (128, ig.PATH_MMA)]:
+        p = ig.plan_query(ig.make_shape(256, 4096, 4096, r, num_adapters=8))
+        assert p["path"] == want, r
+        if want == ig.PATH_MMA:
+            assert p["shrink_bm"] == 128 and p["apply_kernels"] == 2
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_mma_small_integers_bit_exact(mode):
+    # |x A| sums <= 4096 * 16 < 2^24; expand sums < 2^24: every order is exact
+    p = synth.make_problem(300, 4096, 512, 64, slices=1, L=5, seed=31, dist="int",
+                           device="cuda")
+    z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
+    check_shrink(p.to("cpu"), z, exact=True)
+    check_expand(p.to("cpu"), z, y, exact=True)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+@pytest.mark.parametrize("r", [32, 64, 128])
+def test_mma_normal_inputs(mode, r):
+    p = synth.make_problem(200, 2048, 768, r, slices=2, L=3, seed=r, none_frac=0.1,
+                           device="cuda")
+    z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
+    check_shrink(p.to("cpu"), z)
+    check_expand(p.to("cpu"), z, y)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+@pytest.mark.parametrize("r", [16, 48, 64])
+def test_mma_ragged_partition_and_small_ranks(mode, r):
+    # K/S = 1376: the last k-step of each partition has 32 of 64 columns;
+    # r = 16 and 48 are not multiples of one 32-column accumulator read
+    p = synth.make_problem(150, 11008, 264, r, L=4, seed=5 + r, device="cuda")
+    z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
+    check_shrink(p.to("cpu"), z)
+    check_expand(p.to("cpu"), z, y)
+
+
+def test_mma_decode_rows_in_big_tiles():
+    # a few tokens per adapter: tiles of 128 rows mostly empty
+    for M in (1, 5, 33):
+        p = synth.make_problem(M, 8192, 1024, 128, L=4, seed=M, device="cuda")
+        z, y = run_apply(p, mode=ig.MODE_DET, split_k=16, path=ig.PATH_MMA)
+        check_shrink(p.to("cpu"), z)
+        check_expand(p.to("cpu"), z, y)
+
+
+def test_mma_replay_bitwise():
+    p = synth.make_problem(512, 4096, 1024, 64, L=8, seed=9, device="cuda")
+    z0, y0 = run_apply(p, mode=ig.MODE_DET)
+    for _ in range(50):
+        z, y = run_apply(p, mode=ig.MODE_DET)
+        assert torch.equal(z.view(torch.int32), z0.view(torch.int32))
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
