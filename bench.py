@@ -294,6 +294,79 @@ def kernel_durations(ig, st, ws, steps):
     return out
 
 
+PREFILL = [
+    # name, M, K, N, r, slices, L, adapter ids, S, instances
+    ("qkv_M4096_K4096_r64_3x4096", 4096, 4096, 4096, 64, 3, 16, "segments", 8, 2),
+    ("down_M4096_K11008_r64_N4096", 4096, 11008, 4096, 64, 1, 16, "segments", 8, 2),
+    ("large_M8192_K8192_r128_N8192", 8192, 8192, 8192, 128, 1, 64, "zipf", 16, 2),
+    ("large_M8192_K28672_r128_N8192", 8192, 28672, 8192, 128, 1, 64, "zipf", 16, 1),
+]
+
+
+def prefill_bench(ig, device, steps):
+    """Prefill shapes on the tensor-core path: per lora_apply time, algorithmic
+    HBM GB/s and TFLOP/s, and the shrink / expand split (each kernel alone in
+    its own graph). Distinct instances per shape keep the inputs out of L2."""
+    import synth
+    out = {}
+    peak, kind = measured_peaks()
+    for name, M, K, N, r, sl, L, ids, S, inst in PREFILL:
+        probs = [synth.make_problem(M, K, N, r, slices=sl, L=L, ids=ids, segment=256,
+                                    seed=4000 + i, device=device) for i in range(inst)]
+        sh = ig.make_shape(M, K, N, r, slices=sl, num_adapters=L, split_k=S, mode=ig.MODE_DET,
+                           flags=ig.FLAG_STATIC_WEIGHTS)
+        info = ig.plan_query(sh)
+        ws = ig.workspace(sh, device=device)
+        z = torch.empty((sl, M, r), dtype=torch.float32, device=device)
+        ig.map_tokens(sh, probs[0].idx, ws)
+        u = int(torch.unique(probs[0].idx).numel())
+        b = alg_bytes(M, K, N, r, sl, u)
+        flops = 2 * M * K * r * sl + 2 * M * r * N * sl
+        res = {"path": "tcgen05" if info["path"] == ig.PATH_MMA else "fma"}
+        for part in ("apply", "shrink", "expand"):
+            def body(stream, part=part):
+                for p in probs:
+                    if part == "apply":
+                        ig.lora_apply(sh, p.x, p.y, None, p.A, p.B, p.scale, z, ws, stream)
+                    elif part == "shrink":
+                        ig.lora_shrink(sh, p.x, p.A, None, p.scale, z, ws, stream)
+                    else:
+                        ig.lora_expand(sh, z, p.B, None, p.y, ws, stream)
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                body(st)
+            torch.cuda.current_stream().wait_stream(st)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(torch.cuda.current_stream())
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (steps * inst)
+            nbytes = b["total"] if part == "apply" else b[part]
+            nfl = flops if part == "apply" else (2 * M * K * r * sl if part == "shrink"
+                                                 else 2 * M * r * N * sl)
+            res[part] = {"us": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
+                         "hbm_frac_of_" + kind: nbytes / (us * 1e-6) / 1e9 / peak,
+                         "tflops": nfl / (us * 1e-6) / 1e12,
+                         "tokens_per_s": M / (us * 1e-6)}
+            del g
+        assert ig.check_status(ws) == 0
+        out[name] = res
+        del probs, ws, z
+        torch.cuda.empty_cache()
+    return out
+
+
 def source_hash(name):
     path = os.path.join(ROOT, "invariant_gemm_gb300", "csrc", name)
     try:
@@ -409,6 +482,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -536,12 +610,15 @@ def main():
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "how": "pinned host x, y, idx -> device; captured step (C-ABI calls) -> y back"}
 
+    prefill = {} if args.no_prefill else prefill_bench(ig, device, max(5, args.steps // 40))
+
     out = {"metric": METRIC, "value": det["tokens_per_s"], "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": det["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic", "config": workload_config(), "clocks": clk,
            "gpu_launches": launches * args.steps,
-           "roofline": roofline, "variants": results, "sweep_M": sweep, "e2e": e2e,
+           "roofline": roofline, "variants": results, "sweep_M": sweep, "prefill": prefill,
+           "e2e": e2e,
            "hbm_gbs": det["hbm_gbs"]}
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline_obj(args.cpu_seconds)

@@ -128,6 +128,9 @@ int run_shrink_mma(const ig_shape* sh, const Plan& pl, const void* x, const void
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
                          1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
+  rc = encode_map_2d(&p.tm_xt, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
+                     kMmaTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)sh->r,
                      CU_TENSOR_MAP_SWIZZLE_128B);
@@ -153,11 +156,15 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
                    uint8_t* ws, cudaStream_t st) {
   MmaExpandParams p;
   int rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N,
-                         (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, 256,
+                         (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, kMmaExpandCols,
                          CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_y, y, (uint64_t)sh->M, (uint64_t)sh->slices * sh->N,
                      (uint64_t)sh->slices * sh->N * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
+  rc = encode_map_2d(&p.tm_yt, y, (uint64_t)sh->M, (uint64_t)sh->slices * sh->N,
+                     (uint64_t)sh->slices * sh->N * 2, 64, kMmaTileRows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   p.z = z;
   p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
@@ -168,7 +175,7 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
   p.r = sh->r;
   p.slices = sh->slices;
   p.L = sh->num_adapters;
-  p.ntiles = pl.ntiles;
+  p.ntiles = (int)((sh->N + kMmaExpandCols - 1) / kMmaExpandCols);
   p.flags = sh->flags;
   return cuda_status(launch_expand_mma(p, pl.tiles, st));
 }

@@ -8,13 +8,15 @@
 // BF16, rounded to nearest).
 //
 // Block = 4 warps, tile = up to 128 token rows of one adapter (128-row tile
-// table) x 256 output columns of one slice. The A operand of the MMA is the
+// table) x 128 output columns of one slice (64 KB of shared memory at r = 64,
+// so that three blocks share an SM and overlap their copies and epilogues). The A operand of the MMA is the
 // tile's Z rows rounded to bf16, written by the threads straight into the
-// 128-byte-swizzled K-major layout; the B operand is B_i's 256 rows x r,
+// 128-byte-swizzled K-major layout; the B operand is B_i's 128 rows x r,
 // brought by tiled TMA copies (64 rank columns each; columns past r read as
-// zero). The y tile (128 rows x
-// 256 columns) is gathered by TMA into swizzled shared memory while the MMA
-// runs. tcgen05.mma, M = 128, N = 256, K = 16 per instruction, r/16 of them,
+// zero). The y tile (128 rows x 128 columns) is copied by TMA (one box per 64
+// columns when the tile's tokens are consecutive, else row gathers) into
+// swizzled shared memory while the MMA runs. tcgen05.mma, M = 128, N = 128,
+// K = 16 per instruction, r/16 of them,
 // FP32 in tensor memory. Each thread then reads its row of the accumulator,
 // adds it to y in FP32 and rounds once to bf16 in shared memory; a final pass
 // writes y back with whole rows per warp.
@@ -28,7 +30,8 @@ namespace ig {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kBN = 256;                         // output columns per block
+constexpr int kBN = kMmaExpandCols;              // output columns per block (128)
+constexpr int kYBlocks = kBN / 64;               // 64-column blocks of the y tile
 constexpr int kYBlockBytes = kMmaTileRows * 128; // one 64-column block of the y tile
 
 struct Ctl {
@@ -40,11 +43,14 @@ struct Ctl {
 };
 
 // layout (offsets from the 1024-aligned base): ctl 1024, tile entry 1024,
-// then zb [r/64][128 rows][128 B], B [r/64][256 rows][128 B], y [4][128][128 B]
+// then zb [r/64][128 rows][128 B], B [r/64][128 rows][128 B], y [2][128][128 B]
+constexpr int kBAtomBytes = kBN * 128;
 __host__ __device__ inline size_t off_zb() { return 2048; }
 __host__ __device__ inline size_t off_b(int r) { return off_zb() + (size_t)((r + 63) / 64) * 16384; }
-__host__ __device__ inline size_t off_y(int r) { return off_b(r) + (size_t)((r + 63) / 64) * 32768; }
-__host__ __device__ inline size_t mma_expand_smem(int r) { return 1024 + off_y(r) + 4 * kYBlockBytes; }
+__host__ __device__ inline size_t off_y(int r) { return off_b(r) + (size_t)((r + 63) / 64) * kBAtomBytes; }
+__host__ __device__ inline size_t mma_expand_smem(int r) {
+  return 1024 + off_y(r) + kYBlocks * kYBlockBytes;
+}
 
 __global__ void __launch_bounds__(kThreads)
     expand_mma_kernel(const __grid_constant__ MmaExpandParams p) {
@@ -100,24 +106,30 @@ __global__ void __launch_bounds__(kThreads)
   const int b_row = (int)(((int64_t)g * p.slices + sl) * N + n0);
   const int y_col = (int)((int64_t)sl * N + n0);
   const int groups4 = (nrows + 3) / 4;
+  const bool contiguous = ent_s[2] != 0;   // rows are consecutive tokens: one box
   const bool early_b = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
 
   auto issue_b = [&]() {
     for (int a = 0; a < ka; ++a)
-      tma_load_2d(s_b + a * 32768, &p.tm_b, a * 64, b_row, &ctl->bar_b);
+      tma_load_2d(s_b + a * kBAtomBytes, &p.tm_b, a * 64, b_row, &ctl->bar_b);
   };
   if (tid == 0) {
-    mbar_arrive_expect_tx(&ctl->bar_b, (uint32_t)ka * 32768);
-    mbar_arrive_expect_tx(&ctl->bar_y, (uint32_t)groups4 * 4 * 128 * 4);
+    mbar_arrive_expect_tx(&ctl->bar_b, (uint32_t)ka * kBAtomBytes);
+    mbar_arrive_expect_tx(&ctl->bar_y, contiguous ? (uint32_t)kYBlocks * kYBlockBytes
+                                                  : (uint32_t)groups4 * 4 * 128 * kYBlocks);
     if (early_b) issue_b();
   }
   griddep_wait();
   griddep_launch();
   if (tid == 0 && !early_b) issue_b();
-  // y tile: 4 column blocks x row gathers (warp 0 spreads them over lanes)
-  if (warp == 0) {
+  // y tile: 64-column blocks, each one box (consecutive tokens) or row
+  // gathers spread over the lanes of warp 0
+  if (warp == 0 && contiguous) {
+    if (lane < kYBlocks)
+      tma_load_2d(s_y + lane * kYBlockBytes, &p.tm_yt, y_col + lane * 64, rows_s[0], &ctl->bar_y);
+  } else if (warp == 0) {
     const int last = nrows - 1;
-    for (int q = lane; q < groups4 * 4; q += 32) {
+    for (int q = lane; q < groups4 * kYBlocks; q += 32) {
       const int cb = q / groups4, g4 = q % groups4;
       tma_gather4(s_y + cb * kYBlockBytes + g4 * 512, &p.tm_y, y_col + cb * 64,
                   rows_s[min(4 * g4, last)], rows_s[min(4 * g4 + 1, last)],
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int k = 0; k < r / 16; ++k) {
         const int a = k / 4, kk = k % 4;
         umma_bf16(tmem, umma_desc_sw128(smem_u32(s_zb + a * 16384) + kk * 32),
-                  umma_desc_sw128(smem_u32(s_b + a * 32768) + kk * 32), idesc, k > 0);
+                  umma_desc_sw128(smem_u32(s_b + a * kBAtomBytes) + kk * 32), idesc, k > 0);
       }
     } else {
       ctl->fail = 1;
@@ -202,13 +214,15 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
 
-  // epilogue 2: whole rows per warp-instruction back to global memory
+  // epilogue 2: two whole rows (256 bytes each) per warp-instruction back to
+  // global memory
   if (acc_ok && y_ok) {
     const int64_t ld = (int64_t)p.slices * N;
     const int64_t ncols = min((int64_t)kBN, N - n0);
-    for (int m = warp; m < nrows; m += 4) {
-      const int ch = lane;                 // 16-byte chunk of the 512-byte row
-      if ((int64_t)ch * 8 >= ncols) continue;
+    for (int m0 = 2 * warp; m0 < nrows; m0 += 8) {
+      const int m = m0 + lane / 16;
+      const int ch = lane % 16;            // 16-byte chunk of the 256-byte row
+      if (m >= nrows || (int64_t)ch * 8 >= ncols) continue;
       const int cb = ch / 8, c = ch % 8;
       const uint4 u =
           *reinterpret_cast<const uint4*>(s_y + cb * kYBlockBytes + m * 128 + ((c ^ (m & 7)) * 16));

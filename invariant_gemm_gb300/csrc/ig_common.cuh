@@ -57,6 +57,7 @@ static_assert(kExpandBM == kTileRows, "tile rows");
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
+constexpr int kMmaExpandCols = 128;    // output columns per tensor-core expand block
 
 // Tile count over token groups: sum over groups g of ceil(count_g / bm),
 // bounded by floor(M / bm) + (number of non-empty groups).
@@ -126,6 +127,7 @@ struct FusedParams {
 
 struct MmaShrinkParams {
   CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_xt;    // x [M][K], box 64 x 128, 128-byte swizzle (contiguous tiles)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
   const int32_t* tiles; // 128-row tile table
   float* z;
@@ -138,8 +140,9 @@ struct MmaShrinkParams {
 };
 
 struct MmaExpandParams {
-  CUtensorMap tm_b;     // B_stack as [L*slices*N][r], box 64 x 256, 128-byte swizzle
+  CUtensorMap tm_b;     // B_stack as [L*slices*N][r], box 64 x 128, 128-byte swizzle
   CUtensorMap tm_y;     // y [M][slices*N], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_yt;    // y [M][slices*N], box 64 x 128, 128-byte swizzle (contiguous tiles)
   const float* z;
   const int32_t* tiles; // 128-row tile table
   __nv_bfloat16* y;

@@ -20,8 +20,10 @@
 // Finally it writes the tile table the shrink and expand kernels read: group
 // g is cut into ceil(count_g / T) tiles of at most T consecutive rows of the
 // grouped order (T = 16 for the CUDA-core kernels, 128 for the tensor-core
-// ones); tile entries hold [g, nrows, 0, 0, rows[T]] so that a block learns
-// its adapter and its token rows with one contiguous load. Tiles of
+// ones); tile entries hold [g, nrows, contiguous, 0, rows[T]] so that a block
+// learns its adapter and its token rows with one contiguous load.
+// `contiguous` is 1 when the rows are consecutive token indices (then a
+// tile can be copied as one box instead of row by row). Tiles of
 // adapters 0..L-1 come first (in adapter order), then the no-adapter group,
 // then empty entries (nrows = 0) up to tiles_max.
 //
@@ -171,10 +173,18 @@ __global__ void __launch_bounds__(kMapThreads) map_tokens_kernel(MapParams p) {
     const int q = (int)(t - tstart[g]);
     const int first = total[g] + q * T;                   // total[] holds group starts
     const int cnt = min(T, total[g] + cntg[g] - first);
+    const int r0 = p.perm[first];
+    bool consec = true;
+    for (int i = lane; i < T; i += 32) {
+      const int v = i < cnt ? p.perm[first + i] : 0;
+      ent[4 + i] = v;
+      if (i < cnt && v != r0 + i) consec = false;
+    }
+    consec = __all_sync(0xffffffffu, consec);
     if (lane == 0) ent[0] = g;
     if (lane == 1) ent[1] = cnt;
-    if (lane == 2 || lane == 3) ent[lane] = 0;
-    for (int i = lane; i < T; i += 32) ent[4 + i] = i < cnt ? p.perm[first + i] : 0;
+    if (lane == 2) ent[2] = consec ? 1 : 0;
+    if (lane == 3) ent[3] = 0;
   }
 }
 

@@ -15,9 +15,10 @@
 //
 // Block = 4 warps, tile = up to 128 token rows of one adapter (one entry of
 // the token map's 128-row tile table) x all r rank columns. One thread of
-// warp 0 issues the TMA copies: per k-step of 64 elements, row gathers of x
-// (4 rows each, only the tile's rows) and one tiled copy of the A block
-// (r rows), both 128-byte swizzled, into a 4-deep ring. One thread of warp 1
+// warp 0 issues the TMA copies: per k-step of 64 elements, x as one 128-row
+// box when the tile's tokens are consecutive (else row gathers, 4 rows each,
+// only the tile's rows) and one tiled copy of the A block (r rows), all
+// 128-byte swizzled, into a 4-deep ring. One thread of warp 1
 // issues per k-step four tcgen05.mma (M = 128 tokens, N = r, K = 16) into an
 // FP32 accumulator in tensor memory and commits each stage back to the
 // producer. The last k-step of a partition that is not a multiple of 64
@@ -127,7 +128,9 @@ __global__ void __launch_bounds__(kThreads)
   const int nk = (int)((Ks + kKStep - 1) / kKStep);      // k-steps
   const int a_row = (int)(((int64_t)g * p.slices + sl) * r);
   const int groups4 = (nrows + 3) / 4;
-  const uint32_t stage_tx = (uint32_t)groups4 * 4 * 128 + (uint32_t)r * 128;
+  const bool contiguous = ent_s[2] != 0;   // rows are consecutive tokens: one box
+  const uint32_t stage_tx =
+      (contiguous ? (uint32_t)kXTileBytes : (uint32_t)groups4 * 4 * 128) + (uint32_t)r * 128;
   const bool early_a = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
   const int first = min(nk, kStages);
 
@@ -137,6 +140,10 @@ __global__ void __launch_bounds__(kThreads)
   };
   auto issue_x = [&](int b) {
     uint8_t* st = ring + (b % kStages) * stage_bytes;
+    if (contiguous) {
+      tma_load_2d(st, &p.tm_xt, k0 + b * kKStep, rows_s[0], &ctl->full[b % kStages]);
+      return;
+    }
     const int last = nrows - 1;
     for (int q = 0; q < groups4; ++q)
       tma_gather4(st + q * 4 * 128, &p.tm_x, k0 + b * kKStep, rows_s[min(4 * q, last)],

@@ -78,3 +78,20 @@ def test_mma_replay_bitwise():
         z, y = run_apply(p, mode=ig.MODE_DET)
         assert torch.equal(z.view(torch.int32), z0.view(torch.int32))
         assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
+def test_mma_contiguous_tiles_with_overhang(mode):
+    """Tiles whose tokens are consecutive are copied as one 128-row box; the
+    last tile of a single-adapter batch of 300 rows reaches past row M."""
+    p = synth.make_problem(300, 4096, 520, 64, slices=2, L=1, ids="single", seed=77,
+                           device="cuda")
+    z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
+    check_shrink(p.to("cpu"), z)
+    check_expand(p.to("cpu"), z, y)
+    # segments of 256 tokens per adapter (the prefill layout) with a ragged end
+    p = synth.make_problem(700, 4096, 512, 64, L=3, ids="segments", segment=256, seed=78,
+                           device="cuda")
+    z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
+    check_shrink(p.to("cpu"), z)
+    check_expand(p.to("cpu"), z, y)
