@@ -15,6 +15,8 @@
  *     order, multiplies by the scale, writes the tile and resets the counter.
  *   - sec. 4.1: the atomic Split-K baseline adds partials with FP32 atomics.
  *   - sec. 4.2: the unsplit baseline (Split-K = 1) uses one block per tile.
+ *   - sec. 4.3: an earlier deterministic design combined the partials in a
+ *     separate kernel with a fixed pairwise tree (IG_MODE_DET_TREE).
  *   - sec. 6.2 / Fig. 5: the FP32 shrink output is rounded to BF16
  *     (round-to-nearest, ties to even) where the next operation reads it.
  *
@@ -49,7 +51,8 @@
  *     has completed; only the token map (which is always complete before any
  *     later kernel starts) and, with IG_FLAG_STATIC_WEIGHTS, A_stack/B_stack
  *     are read earlier.
- *   - Determinism: in IG_MODE_DET and IG_MODE_UNSPLIT the bits of each z row
+ *   - Determinism: in IG_MODE_DET, IG_MODE_DET_TREE and IG_MODE_UNSPLIT the
+ *     bits of each z row
  *     and y row are a function of that row's inputs, its adapter and the plan
  *     only. The plan (ig_plan_query) is a function of
  *     (K, r, N, slices, split_k, mode, path) and never of M, so results do not
@@ -86,7 +89,11 @@ typedef enum ig_mode {
   IG_MODE_DET = 0,     /* Split-K with FP32 partials in the workspace and a
                           last-arriver fixed-order combine (Algorithm 1) */
   IG_MODE_ATOMIC = 1,  /* Split-K with FP32 atomic adds into a zeroed z */
-  IG_MODE_UNSPLIT = 2  /* Split-K = 1: one block per output tile */
+  IG_MODE_UNSPLIT = 2, /* Split-K = 1: one block per output tile */
+  IG_MODE_DET_TREE = 3 /* Split-K with FP32 partials in the workspace, summed by
+                          a second kernel with a fixed pairwise tree
+                          ((P0+P1)+(P2+P3))+...: the earlier deterministic
+                          design the pages describe in sec. 4.3 */
 } ig_mode;
 
 /* Arithmetic path. It is part of the determinism key: the same request on
@@ -123,6 +130,14 @@ typedef struct ig_shape {
                                     and the expand as two kernels even where
                                     the fused one-launch kernel applies. Both
                                     give the same bits. */
+#define IG_FLAG_Z_FP32 4         /* The expand reads Z in FP32 instead of
+                                    rounding it to bf16 first (sec. 6.2 shows
+                                    the bf16 boundary turning tiny FP32
+                                    differences into visible ones). CUDA-core
+                                    path: Z is used as stored. Tensor-core
+                                    path: Z = hi + lo with hi = bf16_rn(Z),
+                                    lo = bf16_rn(Z - hi), two MMAs per K step
+                                    (16 significant bits of Z). */
 
 /* The resolved plan. Everything that fixes the arithmetic is in
  * determinism_key, which never depends on M. */
@@ -189,6 +204,8 @@ int lora_shrink(const ig_shape* shape, const void* x, const void* A_stack,
 /* Expand (Eq. 1, sec. 6.2):
  *   y[m][sl*N + n] = bf16_rn( f32(y[m][sl*N+n])
  *                             + sum_{j<r} bf16_rn(z[sl][m][j]) * B_stack[a_m][sl][n][j] )
+ * (with IG_FLAG_Z_FP32: z[sl][m][j] itself, or its hi/lo bf16 pair on the
+ * tensor-core path, instead of bf16_rn(z))
  * The sum over j is a sequential FP32 chain in increasing j; y is rounded
  * once. Rows with adapter -1 are not written. adapter_idx may be NULL to
  * reuse the token map in ws. */

@@ -19,17 +19,18 @@ import ctypes
 import os
 
 __all__ = [
-    "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "PATH_AUTO", "PATH_FMA", "PATH_MMA",
-    "FLAG_STATIC_WEIGHTS", "FLAG_UNFUSED",
+    "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "MODE_DET_TREE", "PATH_AUTO", "PATH_FMA", "PATH_MMA",
+    "FLAG_STATIC_WEIGHTS", "FLAG_UNFUSED", "FLAG_Z_FP32",
     "IGError", "Shape", "PlanInfo", "lib", "lib_path", "make_shape", "workspace_bytes",
     "plan_query", "workspace", "workspace_init", "map_tokens", "lora_shrink",
     "lora_expand", "lora_apply", "lora_shrink_noalloc", "check_status", "status_string",
     "EXPORTS",
 ]
 
-MODE_DET, MODE_ATOMIC, MODE_UNSPLIT = 0, 1, 2
+MODE_DET, MODE_ATOMIC, MODE_UNSPLIT, MODE_DET_TREE = 0, 1, 2, 3
 FLAG_STATIC_WEIGHTS = 1
 FLAG_UNFUSED = 2
+FLAG_Z_FP32 = 4
 PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 
 STATUS = {

@@ -35,8 +35,9 @@ uint64_t fnv1a(uint64_t h, int64_t v) {
 
 int make_plan(const ig_shape* sh, Plan* pl) {
   if (!sh || !pl) return IG_ERR_ARG;
-  if ((sh->flags & ~(IG_FLAG_STATIC_WEIGHTS | IG_FLAG_UNFUSED)) != 0) return IG_ERR_ARG;
-  if (sh->mode < IG_MODE_DET || sh->mode > IG_MODE_UNSPLIT) return IG_ERR_ARG;
+  if ((sh->flags & ~(IG_FLAG_STATIC_WEIGHTS | IG_FLAG_UNFUSED | IG_FLAG_Z_FP32)) != 0)
+    return IG_ERR_ARG;
+  if (sh->mode < IG_MODE_DET || sh->mode > IG_MODE_DET_TREE) return IG_ERR_ARG;
   if (sh->path < IG_PATH_AUTO || sh->path > IG_PATH_MMA) return IG_ERR_ARG;
   const int64_t M = sh->M, K = sh->K, N = sh->N, r = sh->r;
   if (M < 0 || K < 8 || N < 8 || r < 8) return IG_ERR_SHAPE;
@@ -69,7 +70,9 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   pl->tiles = tiles_upper_bound(M, L + 1, pl->tile_rows);
   pl->ntiles = (int)((N + kExpandBN - 1) / kExpandBN);
   const int64_t slots = pl->tiles * sh->slices * pl->jblocks;
+  const bool partials = sh->mode == IG_MODE_DET || sh->mode == IG_MODE_DET_TREE;
   if (sh->mode == IG_MODE_DET && slots > kMaxCounters) return IG_ERR_UNSUPPORTED;
+  if (sh->mode == IG_MODE_DET_TREE && S > 64) return IG_ERR_UNSUPPORTED;
 
   pl->off_perm = kMapOffset;
   pl->off_offsets = align_up(pl->off_perm + 4 * (size_t)M, 256);
@@ -77,8 +80,7 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   pl->off_partials =
       align_up(pl->off_tiles + 4 * (size_t)(4 + pl->tile_rows) * pl->tiles, 256);
   size_t part = 0;
-  if (sh->mode == IG_MODE_DET)
-    part = (size_t)slots * S * pl->tile_rows * pl->bn * sizeof(float);
+  if (partials) part = (size_t)slots * S * pl->tile_rows * pl->bn * sizeof(float);
   pl->total = align_up(pl->off_partials + part, 256);
 
   pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_FMA && (r == 8 || r == 16) &&
@@ -87,7 +89,7 @@ int make_plan(const ig_shape* sh, Plan* pl) {
 
   uint64_t h = 1469598103934665603ull;
   const int64_t fields[] = {IG_ABI_VERSION, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
-                            pl->bn, mma ? 64 : kShrinkKB};
+                            pl->bn, mma ? 64 : kShrinkKB, sh->flags & IG_FLAG_Z_FP32};
   for (int64_t f : fields) h = fnv1a(h, f);
   pl->key = h;
   return IG_OK;
@@ -180,8 +182,36 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
   return cuda_status(launch_expand_mma(p, pl.tiles, st));
 }
 
+int run_tree(const ig_shape* sh, const Plan& pl, float scale, float* z, uint8_t* ws,
+             cudaStream_t st) {
+  TreeParams p;
+  p.partials = reinterpret_cast<const float*>(ws + pl.off_partials);
+  p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
+  p.z = z;
+  p.M = sh->M;
+  p.r = sh->r;
+  p.tile_rows = pl.tile_rows;
+  p.bn = pl.bn;
+  p.jblocks = pl.jblocks;
+  p.slices = sh->slices;
+  p.L = sh->num_adapters;
+  p.S = pl.S;
+  p.scale = scale;
+  return cuda_status(launch_reduce_tree(p, pl.tiles, st));
+}
+
+int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
+                    float scale, float* z, uint8_t* ws, cudaStream_t st);
+
 int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A, float scale,
                float* z, uint8_t* ws, cudaStream_t st) {
+  const int rc = run_shrink_only(sh, pl, x, A, scale, z, ws, st);
+  if (rc != IG_OK || pl.mode != IG_MODE_DET_TREE) return rc;
+  return run_tree(sh, pl, scale, z, ws, st);
+}
+
+int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
+                    float scale, float* z, uint8_t* ws, cudaStream_t st) {
   if (pl.mode == IG_MODE_ATOMIC) {
     cudaError_t e = cudaMemsetAsync(z, 0, sizeof(float) * sh->slices * sh->M * sh->r, st);
     if (e != cudaSuccess) return IG_ERR_CUDA;

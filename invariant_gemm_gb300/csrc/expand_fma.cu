@@ -89,10 +89,12 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
   for (int i = 0; i < RW; ++i)
     if (active && m[i] >= 0)
       yv[i] = *reinterpret_cast<const uint4*>(p.y + (int64_t)m[i] * ld + (int64_t)sl * N + n);
-  // The tile's Z rows for one rank chunk, rounded to bf16 and kept as packed
-  // pairs (every lane loads the same addresses: one transaction per warp; L2
-  // only, Z was written by the previous kernel).
-  uint32_t zp[RW][JC / 2];
+  // The tile's Z rows for one rank chunk, rounded to bf16 (as FP32 values;
+  // with IG_FLAG_Z_FP32 left as stored). Every lane loads the same
+  // addresses: one transaction per warp; L2 only, Z was written by the
+  // previous kernel.
+  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
+  float zf[RW][JC];
   auto load_z = [&](int jc) {
 #pragma unroll
     for (int i = 0; i < RW; ++i) {
@@ -102,8 +104,10 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
 #pragma unroll
       for (int q = 0; q < JC / 4; ++q) {
         const float4 f = __ldcg(zsrc + q);
-        zp[i][2 * q] = f32_to_bf16_bits(f.x) | (f32_to_bf16_bits(f.y) << 16);
-        zp[i][2 * q + 1] = f32_to_bf16_bits(f.z) | (f32_to_bf16_bits(f.w) << 16);
+        zf[i][4 * q + 0] = zf32 ? f.x : bf16_round_f32(f.x);
+        zf[i][4 * q + 1] = zf32 ? f.y : bf16_round_f32(f.y);
+        zf[i][4 * q + 2] = zf32 ? f.z : bf16_round_f32(f.z);
+        zf[i][4 * q + 3] = zf32 ? f.w : bf16_round_f32(f.w);
       }
     }
   };
@@ -130,9 +134,8 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
       float zq[RW][8];
 #pragma unroll
       for (int i = 0; i < RW; ++i)
-        if (m[i] >= 0)
-          unpack8(make_uint4(zp[i][4 * q], zp[i][4 * q + 1], zp[i][4 * q + 2], zp[i][4 * q + 3]),
-                  zq[i]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zq[i][e] = zf[i][8 * q + e];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         float bf[8];

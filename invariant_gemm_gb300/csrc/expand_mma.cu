@@ -45,11 +45,16 @@ struct Ctl {
 // layout (offsets from the 1024-aligned base): ctl 1024, tile entry 1024,
 // then zb [r/64][128 rows][128 B], B [r/64][128 rows][128 B], y [2][128][128 B]
 constexpr int kBAtomBytes = kBN * 128;
+// (with FP32 Z: zb holds the hi atoms, then the lo atoms)
 __host__ __device__ inline size_t off_zb() { return 2048; }
-__host__ __device__ inline size_t off_b(int r) { return off_zb() + (size_t)((r + 63) / 64) * 16384; }
-__host__ __device__ inline size_t off_y(int r) { return off_b(r) + (size_t)((r + 63) / 64) * kBAtomBytes; }
-__host__ __device__ inline size_t mma_expand_smem(int r) {
-  return 1024 + off_y(r) + kYBlocks * kYBlockBytes;
+__host__ __device__ inline size_t off_b(int r, bool zf32) {
+  return off_zb() + (size_t)((r + 63) / 64) * 16384 * (zf32 ? 2 : 1);
+}
+__host__ __device__ inline size_t off_y(int r, bool zf32) {
+  return off_b(r, zf32) + (size_t)((r + 63) / 64) * kBAtomBytes;
+}
+__host__ __device__ inline size_t mma_expand_smem(int r, bool zf32) {
+  return 1024 + off_y(r, zf32) + kYBlocks * kYBlockBytes;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -60,9 +65,10 @@ __global__ void __launch_bounds__(kThreads)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 1024);
   const int r = (int)p.r;
+  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
   uint8_t* s_zb = smem + off_zb();
-  uint8_t* s_b = smem + off_b(r);
-  uint8_t* s_y = smem + off_y(r);
+  uint8_t* s_b = smem + off_b(r, zf32);
+  uint8_t* s_y = smem + off_y(r, zf32);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int64_t bid = blockIdx.x;
@@ -139,25 +145,36 @@ __global__ void __launch_bounds__(kThreads)
 
   // A operand: this thread's Z row (token row `tid` of the tile), rounded to
   // bf16, into the swizzled K-major layout (16-byte chunk c of a 128-byte row
-  // m sits at chunk c ^ (m % 8)).
+  // m sits at chunk c ^ (m % 8)). With FP32 Z also the remainder
+  // lo = bf16_rn(z - hi), in atoms after the hi ones.
   {
     const int m = tid;
     const bool valid = m < nrows;
     const float* zr = p.z + ((int64_t)sl * M + (valid ? rows_s[m] : 0)) * r;
     for (int a = 0; a < ka; ++a) {
       uint8_t* rowp = s_zb + a * 16384 + m * 128;
+      uint8_t* lowp = s_zb + (ka + a) * 16384 + m * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint4 w = make_uint4(0, 0, 0, 0);
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0;
         if (valid && a * 64 + c * 8 < r) {
           const float4 f0 = __ldcg(reinterpret_cast<const float4*>(zr + a * 64 + c * 8));
           const float4 f1 = __ldcg(reinterpret_cast<const float4*>(zr + a * 64 + c * 8 + 4));
-          w.x = f32_to_bf16_bits(f0.x) | (f32_to_bf16_bits(f0.y) << 16);
-          w.y = f32_to_bf16_bits(f0.z) | (f32_to_bf16_bits(f0.w) << 16);
-          w.z = f32_to_bf16_bits(f1.x) | (f32_to_bf16_bits(f1.y) << 16);
-          w.w = f32_to_bf16_bits(f1.z) | (f32_to_bf16_bits(f1.w) << 16);
+          const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            hi[e] = f32_to_bf16_bits(f[e]);
+            if (zf32) lo[e] = f32_to_bf16_bits(f[e] - __uint_as_float(hi[e] << 16));
+          }
         }
-        *reinterpret_cast<uint4*>(rowp + ((c ^ (m & 7)) * 16)) = w;
+        const int pc = (c ^ (m & 7)) * 16;
+        *reinterpret_cast<uint4*>(rowp + pc) = make_uint4(
+            hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16), hi[6] | (hi[7] << 16));
+        if (zf32)
+          *reinterpret_cast<uint4*>(lowp + pc) = make_uint4(
+              lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16), lo[4] | (lo[5] << 16), lo[6] | (lo[7] << 16));
       }
     }
   }
@@ -170,8 +187,12 @@ __global__ void __launch_bounds__(kThreads)
       const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, kBN);
       for (int k = 0; k < r / 16; ++k) {
         const int a = k / 4, kk = k % 4;
-        umma_bf16(tmem, umma_desc_sw128(smem_u32(s_zb + a * 16384) + kk * 32),
-                  umma_desc_sw128(smem_u32(s_b + a * kBAtomBytes) + kk * 32), idesc, k > 0);
+        const uint64_t bdesc = umma_desc_sw128(smem_u32(s_b + a * kBAtomBytes) + kk * 32);
+        umma_bf16(tmem, umma_desc_sw128(smem_u32(s_zb + a * 16384) + kk * 32), bdesc, idesc,
+                  k > 0);
+        if (zf32)
+          umma_bf16(tmem, umma_desc_sw128(smem_u32(s_zb + (ka + a) * 16384) + kk * 32), bdesc,
+                    idesc, true);
       }
     } else {
       ctl->fail = 1;
@@ -241,7 +262,7 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st) {
-  const size_t smem = mma_expand_smem((int)p.r);
+  const size_t smem = mma_expand_smem((int)p.r, (p.flags & IG_FLAG_Z_FP32) != 0);
   cudaError_t e = cudaFuncSetAttribute(expand_mma_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -251,6 +272,6 @@ cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaS
   return launch_pdl(expand_mma_kernel, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
 }
 
-size_t expand_mma_smem_bytes(int r) { return mma_expand_smem(r); }
+size_t expand_mma_smem_bytes(int r) { return mma_expand_smem(r, false); }
 
 }  // namespace ig

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     for (int q = 0; q < 16; ++q)
       if (q < S) total += pv[q];
     const float zv = total * p.scale;
-    zs[(o / BN) * ZS + o % BN] = bf16_round_f32(zv);
+    zs[(o / BN) * ZS + o % BN] = (p.flags & IG_FLAG_Z_FP32) ? zv : bf16_round_f32(zv);
     if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
   }
   cluster_arrive();  // done reading the other blocks' partials

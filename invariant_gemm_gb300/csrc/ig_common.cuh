@@ -151,6 +151,15 @@ struct MmaExpandParams {
   int32_t slices, L, ntiles, flags;
 };
 
+struct TreeParams {
+  const float* partials;
+  const int32_t* tiles;
+  float* z;
+  int64_t M, r;
+  int32_t tile_rows, bn, jblocks, slices, L, S;
+  float scale;
+};
+
 // Launchers (defined in the .cu files); they return cudaGetLastError().
 cudaError_t launch_map_tokens(const MapParams& p, cudaStream_t st);
 cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn,
@@ -163,6 +172,7 @@ cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_
                               cudaStream_t st);
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st);
 size_t expand_mma_smem_bytes(int r);
+cudaError_t launch_reduce_tree(const TreeParams& p, int64_t tiles_max, cudaStream_t st);
 
 // Launch helper: programmatic dependent launch on `st` (see griddep_wait).
 template <typename Kern, typename P>

@@ -9,7 +9,8 @@
 //                   multiplies by the scale, writes the tile and zeroes the
 //                   counter;
 //   sec. 4.1        ATOMIC: FP32 atomic add of scale * partial into zeroed Z;
-//   sec. 4.2        UNSPLIT: S = 1, one block over the whole of K.
+//   sec. 4.2        UNSPLIT: S = 1, one block over the whole of K;
+//   sec. 4.3        DET_TREE: partials only, combined by reduce_tree.cu.
 //
 // Block = 16/RPW warps of RPW = 32/BN rows (8 x 2 for BN = 16, 4 x 4 for
 // BN = 8), tile = up to 16 token rows of one adapter (one entry of the token
@@ -143,9 +144,11 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   }
 
   // DET: publish the partial, then the completion-counter protocol.
+  // DET_TREE: publish the partial only; a second kernel combines.
   const int64_t slot = (t * p.slices + sl) * p.jblocks + jb;
   float* part = p.partials + (slot * S) * (kTileRows * BN);
   part[(int64_t)s * (kTileRows * BN) + rrow * BN + j0] = v;
+  if (MODE == IG_MODE_DET_TREE) return;
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -185,10 +188,12 @@ cudaError_t launch_one(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st
 cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn, int64_t tiles_max,
                               cudaStream_t st) {
   if (bn == 16) {
+    if (mode == IG_MODE_DET_TREE) return launch_one<16, IG_MODE_DET_TREE>(p, tiles_max, st);
     if (mode == IG_MODE_DET) return launch_one<16, IG_MODE_DET>(p, tiles_max, st);
     if (mode == IG_MODE_ATOMIC) return launch_one<16, IG_MODE_ATOMIC>(p, tiles_max, st);
     return launch_one<16, IG_MODE_UNSPLIT>(p, tiles_max, st);
   }
+  if (mode == IG_MODE_DET_TREE) return launch_one<8, IG_MODE_DET_TREE>(p, tiles_max, st);
   if (mode == IG_MODE_DET) return launch_one<8, IG_MODE_DET>(p, tiles_max, st);
   if (mode == IG_MODE_ATOMIC) return launch_one<8, IG_MODE_ATOMIC>(p, tiles_max, st);
   return launch_one<8, IG_MODE_UNSPLIT>(p, tiles_max, st);

@@ -11,7 +11,8 @@
 //                   multiplies by the scale, writes the tile, zeroes the
 //                   counter;
 //   sec. 4.1        ATOMIC: FP32 atomic add of scale * partial into zeroed Z;
-//   sec. 4.2        UNSPLIT: S = 1.
+//   sec. 4.2        UNSPLIT: S = 1;
+//   sec. 4.3        DET_TREE: partials only, combined by reduce_tree.cu.
 //
 // Block = 4 warps, tile = up to 128 token rows of one adapter (one entry of
 // the token map's 128-row tile table) x all r rank columns. One thread of
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads)
     tmem_ld32(trow + c, v);
     if (!acc_ok || row >= nrows) continue;
     const int nv = min(32, r - c);   // r is a multiple of 16
-    if (MODE == IG_MODE_DET) {
+    if (MODE == IG_MODE_DET || MODE == IG_MODE_DET_TREE) {
       float4* dst = reinterpret_cast<float4*>(part + (int64_t)s * (kMmaTileRows * r) +
                                               (int64_t)row * r + c);
 #pragma unroll
@@ -246,11 +247,20 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     if ((uint32_t)ctl->info[0] == (uint32_t)(S - 1)) {
       __threadfence();
-      for (int o = tid; o < nrows * r; o += kThreads) {
-        float total = 0.0f;
-        for (int q = 0; q < S; ++q)
-          total += __ldcg(part + (int64_t)q * (kMmaTileRows * r) + o);
-        p.z[((int64_t)sl * M + rows_s[o / r]) * r + o % r] = total * p.scale;
+      // four consecutive columns of one row per step (r is a multiple of 16)
+      for (int o = 4 * tid; o < nrows * r; o += 4 * kThreads) {
+        float4 total = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int q = 0; q < S; ++q) {
+          const float4 v =
+              __ldcg(reinterpret_cast<const float4*>(part + (int64_t)q * (kMmaTileRows * r) + o));
+          total.x += v.x;
+          total.y += v.y;
+          total.z += v.z;
+          total.w += v.w;
+        }
+        *reinterpret_cast<float4*>(p.z + ((int64_t)sl * M + rows_s[o / r]) * r + o % r) =
+            make_float4(total.x * p.scale, total.y * p.scale, total.z * p.scale,
+                        total.w * p.scale);
       }
       if (tid == 0) p.counters[slot] = 0u;
     }
@@ -283,6 +293,7 @@ cudaError_t launch_mode(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_
 cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
                               cudaStream_t st) {
   if (mode == IG_MODE_DET) return launch_mode<IG_MODE_DET>(p, tiles_max, st);
+  if (mode == IG_MODE_DET_TREE) return launch_mode<IG_MODE_DET_TREE>(p, tiles_max, st);
   if (mode == IG_MODE_ATOMIC) return launch_mode<IG_MODE_ATOMIC>(p, tiles_max, st);
   return launch_mode<IG_MODE_UNSPLIT>(p, tiles_max, st);
 }

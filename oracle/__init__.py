@@ -129,7 +129,7 @@ def shrink(x_bits, A_bits, idx, scale):
     return z, bound
 
 
-def expand(z_f32, B_bits, idx, y_bits):
+def expand(z_f32, B_bits, idx, y_bits, round_z=True):
     """y[m, sl*N + n] += sum_j bf16(Z[sl, m, j]) * B[idx[m], sl, n, j]   (Eq. 1).
 
     z_f32   float32 [slices][M][r]   shrink output as stored (FP32)
@@ -137,7 +137,9 @@ def expand(z_f32, B_bits, idx, y_bits):
     idx     int     [M]
     y_bits  uint16  [M][slices*N]    bf16 base output, updated
     Z is first rounded to bf16 (sec. 6.2: the FP32 shrink output reaches the
-    next operation in bf16). Returns (y_exact, bound, y_bits_out):
+    next operation in bf16); with round_z=False the FP32 values are used as
+    they are (the precision variant that keeps Z in FP32).
+    Returns (y_exact, bound, y_bits_out):
       y_exact    float64 value y + sum_j zb_j * B_nj, before the final rounding
       bound      |y| + sum_j |zb_j * B_nj|
       y_bits_out bf16_round(y_exact) for rows with an adapter, y unchanged else
@@ -150,7 +152,10 @@ def expand(z_f32, B_bits, idx, y_bits):
     y_bits = np.asarray(y_bits).astype(np.uint16)
     assert y_bits.shape == (M, slices * N)
     idx = _check_idx(idx, L)
-    zb = bf16_to_f64(bf16_round(z.astype(np.float64)))
+    if round_z:
+        zb = bf16_to_f64(bf16_round(z.astype(np.float64)))
+    else:
+        zb = z.astype(np.float64)
     y = bf16_to_f64(y_bits)
     y_exact = y.copy()
     bound = np.abs(y)

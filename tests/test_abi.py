@@ -62,7 +62,8 @@ def test_plan_independent_of_M():
 
 
 @pytest.mark.parametrize("field,value", [("K", 8192), ("r", 32), ("split_k", 4),
-                                         ("mode", ig.MODE_UNSPLIT), ("slices", 3)])
+                                         ("mode", ig.MODE_UNSPLIT), ("slices", 3),
+                                         ("mode", ig.MODE_DET_TREE)])
 def test_plan_key_changes_with_arithmetic_fields(field, value):
     a = ig.plan_query(shp())["determinism_key"]
     b = ig.plan_query(shp(**{field: value}))["determinism_key"]
@@ -106,8 +107,9 @@ def test_workspace_bytes():
 @pytest.mark.parametrize("kw,code", [
     (dict(K=4100), -2), (dict(N=12), -2), (dict(r=12), -2), (dict(split_k=3), -2),
     (dict(split_k=0), -2), (dict(slices=0), -2), (dict(num_adapters=0), -2),
-    (dict(M=-1), -2), (dict(mode=3), -1), (dict(path=7), -1),
+    (dict(M=-1), -2), (dict(mode=4), -1), (dict(path=7), -1),
     (dict(num_adapters=5000), -9), (dict(r=512), -9),
+    (dict(mode=3, split_k=128), -9),
 ])
 def test_plan_rejects(kw, code):
     with pytest.raises(ig.IGError) as e:

@@ -316,6 +316,28 @@ def test_oracle_expand_pins(pin):
     assert pin(oracle.expand)
 
 
+def test_oracle_expand_fp32_z_bruteforce():
+    """round_z=False: y_exact = y + sum_j z_j B_nj with the FP32 z values as
+    they are (exact rationals, tiny shapes)."""
+    for seed in range(3):
+        x, A, B, y, idx = _tiny(seed)
+        L, slices, N, r = B.shape
+        M = y.shape[0]
+        rng = np.random.default_rng(50 + seed)
+        z32 = (rng.standard_normal((slices, M, r)) * 3).astype(np.float32)
+        y_exact, bound, out = oracle.expand(z32, B, idx, y, round_z=False)
+        for m in range(M):
+            if idx[m] < 0:
+                continue
+            for sl in range(slices):
+                for n in range(N):
+                    exact = frac_of_bits(y[m, sl * N + n]) + sum(
+                        (Fraction(float(z32[sl, m, j])) * frac_of_bits(B[idx[m], sl, n, j])
+                         for j in range(r)), Fraction(0))
+                    got = Fraction(float(y_exact[m, sl * N + n]))
+                    assert abs(got - exact) <= abs(exact) * Fraction(1, 2**50) + Fraction(1, 2**200)
+
+
 def test_oracle_apply_chains_stages():
     x, A, B, y, idx = _tiny(21)
     z32, y_exact, bound, out = oracle.apply(x, y, idx, A, B, 2.0)
