@@ -367,13 +367,58 @@ def prefill_bench(ig, device, steps):
     return out
 
 
+def atomic_replay_stats(ig, st, n):
+    """Identical-input replay of one layer's shrink (sec. 5.2 / 6.1): n runs
+    compared with run 0, for the atomic, deterministic and unsplit modes:
+    share of runs with any differing FP32 output, share of differing
+    elements, mean and max absolute difference."""
+    out = {}
+    for name, mode in (("atomic_sk8", ig.MODE_ATOMIC), ("det_sk8", ig.MODE_DET),
+                       ("unsplit_sk1", ig.MODE_UNSPLIT)):
+        sh = make_shape(ig, st, mode)
+        ws = ig.workspace(sh)
+        z0 = torch.empty_like(st.z)
+        ig.lora_shrink(sh, st.x[0], st.A[0], st.idx, st.scale, z0, ws)
+        z = torch.empty_like(z0)
+        runs = torch.zeros((), dtype=torch.int64, device=z.device)
+        elems = torch.zeros((), dtype=torch.int64, device=z.device)
+        absd = torch.zeros((), dtype=torch.float64, device=z.device)
+        mx = torch.zeros((), dtype=torch.float64, device=z.device)
+        for _ in range(n):
+            ig.lora_shrink(sh, st.x[0], st.A[0], st.idx, st.scale, z, ws)
+            d = (z.view(torch.int32) != z0.view(torch.int32))
+            ne = d.sum()
+            runs += (ne > 0).to(torch.int64)
+            elems += ne
+            ad = (z.double() - z0.double()).abs()
+            absd += ad.sum()
+            mx = torch.maximum(mx, ad.max())
+        assert ig.check_status(ws) == 0
+        ne_total = int(elems)
+        out[name] = {"replays": n, "runs_differing_pct": 100.0 * int(runs) / n,
+                     "elements_differing_pct": 100.0 * ne_total / (n * z0.numel()),
+                     "mean_abs_diff_of_differing": float(absd) / max(1, ne_total),
+                     "max_abs_diff": float(mx)}
+    return out
+
+
+KERNEL_SOURCES = {
+    "fused_fma.cu": ["fused_fma.cu", "shrink_core.cuh", "ig_common.cuh"],
+    "shrink_fma.cu": ["shrink_fma.cu", "shrink_core.cuh", "ig_common.cuh"],
+    "expand_fma.cu": ["expand_fma.cu", "ig_common.cuh"],
+}
+
+
 def source_hash(name):
-    path = os.path.join(ROOT, "invariant_gemm_gb300", "csrc", name)
+    """Hash of the sources a kernel is compiled from (its .cu and headers)."""
+    h = hashlib.sha256()
     try:
-        with open(path, "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
+        for f in KERNEL_SOURCES.get(name, [name]):
+            with open(os.path.join(ROOT, "invariant_gemm_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
     except OSError:
         return None
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_file, workload_key):
@@ -506,7 +551,9 @@ def main():
     ws = {}
     for mode in (ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT):
         ws[mode] = ig.workspace(make_shape(ig, st, mode), device=device)
+    ws[ig.MODE_DET_TREE] = ig.workspace(make_shape(ig, st, ig.MODE_DET_TREE), device=device)
     variants = (("det_sk8", ig.MODE_DET, 0), ("det_sk8_two_kernel", ig.MODE_DET, ig.FLAG_UNFUSED),
+                ("det_tree_sk8_two_launch", ig.MODE_DET_TREE, 0),
                 ("atomic_sk8", ig.MODE_ATOMIC, 0), ("unsplit_sk1", ig.MODE_UNSPLIT, 0))
 
     clocks = ClockSampler(local)
@@ -540,6 +587,8 @@ def main():
         results["det_sk8_two_kernel"]["ms_per_step"] / results["atomic_sk8"]["ms_per_step"] - 1)
     results["det_speedup_vs_unsplit_pct"] = 100 * (results["unsplit_sk1"]["ms_per_step"] /
                                                    det["ms_per_step"] - 1)
+    results["det_tree_overhead_vs_det_pct"] = 100 * (
+        results["det_tree_sk8_two_launch"]["ms_per_step"] / det["ms_per_step"] - 1)
 
     # sweep over the decode batch sizes
     sweep = {}
@@ -557,6 +606,21 @@ def main():
                              "hbm_gbs": b["total"] * W["layers"] / (ms * 1e-3) / 1e9}
                 del g
             sweep[str(M)] = row
+
+    # Split-K sweep of the deterministic path (sec. 4 compares S = 2, 4, 8, 16)
+    split_sweep = {}
+    if not args.no_sweep:
+        for S in (1, 2, 4, 8, 16, 64):
+            sh = ig.make_shape(W["M"], W["K"], W["N"], W["r"], slices=W["slices"],
+                               num_adapters=W["L"], split_k=S, mode=ig.MODE_DET,
+                               flags=ig.FLAG_STATIC_WEIGHTS)
+            wsS = ig.workspace(sh, device=device)
+            g, _ = capture(ig, st, sh, wsS)
+            ms = time_graph(g, max(20, args.steps // 4), 3, world, device)
+            split_sweep[str(S)] = {"us_per_layer": ms * 1e3 / W["layers"],
+                                   "kernels_per_layer": ig.plan_query(sh)["apply_kernels"]}
+            del g, wsS
+    replay = atomic_replay_stats(ig, st, 200)
 
     # dominant kernel roofline: per-launch CUDA-event durations
     kd = kernel_durations(ig, st, ws[ig.MODE_DET], max(20, args.steps // 4))
@@ -617,7 +681,8 @@ def main():
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic", "config": workload_config(), "clocks": clk,
            "gpu_launches": launches * args.steps,
-           "roofline": roofline, "variants": results, "sweep_M": sweep, "prefill": prefill,
+           "roofline": roofline, "variants": results, "sweep_M": sweep, "split_sweep": split_sweep,
+           "atomic_replay": replay, "prefill": prefill,
            "e2e": e2e,
            "hbm_gbs": det["hbm_gbs"]}
     if rank == 0:
