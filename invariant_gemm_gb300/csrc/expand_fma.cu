@@ -11,7 +11,7 @@
 // The j order is fixed and every element is computed by one thread, so the
 // result does not depend on the tiling, on M or on the other rows.
 //
-// Block = 8 warps, tile = up to 16 token rows of one adapter (one entry of
+// Block = 4 warps, tile = up to 8 token rows of one adapter (one entry of
 // the token map's tile table) x 256 output columns of one slice. Lane l owns
 // columns n0 + 8l .. n0 + 8l + 7 (one 16-byte vector of y per row, so a warp
 // reads and writes 512 contiguous bytes of a row); warp w owns rows 2w and
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
   const int sl = (int)(bid % p.slices);
   const int64_t t = bid / p.slices;
 
-  // Tile entry [g, nrows, 0, 0, rows[16]]; complete before this kernel began.
+  // Tile entry [g, nrows, consecutive, 0, rows[8]]; complete before this kernel began.
   const int32_t* ent = p.tiles + t * kTileInts;
   const int g = ent[0];
   const int nrows = ent[1];

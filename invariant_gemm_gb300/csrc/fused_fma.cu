@@ -21,8 +21,8 @@
 // same code (shrink_core.cuh), the combine adds them in the same order, and
 // the expand keeps the same j order and single rounding.
 //
-// Block = 16/RPW warps of RPW = 32/r rows; cluster = S blocks (rank s = K
-// partition s); tile = up to 16 token rows of one adapter (tile-table entry)
+// Block = 8/RPW warps of RPW = 32/r rows; cluster = S blocks (rank s = K
+// partition s); tile = up to 8 token rows of one adapter (tile-table entry)
 // x all r rank columns (r = 8 or 16). Copies: the A block of each k-block by
 // one tiled TMA copy, the token rows of x by row-gather TMA copies (4 rows
 // each), the block's B column slice (contiguous in B_stack) by one bulk copy;

@@ -44,11 +44,11 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) {
 
 // FMA-path geometry (fixed: part of the determinism key where it sets the
 // arithmetic order).
-constexpr int kTileRows = 16;          // token rows per tile of the tile table
-constexpr int kTileInts = 4 + kTileRows;  // [g, nrows, 0, 0, rows[16]] = 80 bytes
+constexpr int kTileRows = 8;           // token rows per tile of the tile table
+constexpr int kTileInts = 4 + kTileRows;  // [g, nrows, consecutive, 0, rows[8]] = 48 bytes
 constexpr int kShrinkKB = 256;        // elements per k-block: 32 lanes x 8
 constexpr int kShrinkStages = 4;
-constexpr int kExpandWarps = 8;
+constexpr int kExpandWarps = 4;
 constexpr int kExpandRowsPerWarp = 2;
 constexpr int kExpandBM = kExpandWarps * kExpandRowsPerWarp;  // 16 = kTileRows
 constexpr int kExpandBN = 256;        // output columns: 32 lanes x 8

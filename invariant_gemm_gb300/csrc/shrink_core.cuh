@@ -2,8 +2,8 @@
 // by the Split-K shrink kernel and the fused decode kernel so that both
 // compute bit-identical partials.
 //
-// Tile: up to 16 token rows x BN rank columns (BN = 8 or 16). The block has
-// 16/RPW warps of RPW = 32/BN rows each, so every lane ends with exactly one
+// Tile: up to 8 token rows x BN rank columns (BN = 8 or 16). The block has
+// 8/RPW warps of RPW = 32/BN rows each, so every lane ends with exactly one
 // finished output. The partition [k0, k0 + Ks) is streamed through a ring of
 // `nst` shared-memory stages, k-blocks of 256 elements, completion counted in
 // bytes on one mbarrier per stage; warp 0 issues the copies. Two ways to
@@ -29,7 +29,7 @@ namespace ig {
 template <int BN>
 struct ShrinkGeo {
   static constexpr int RPW = 32 / BN;             // rows per warp
-  static constexpr int WARPS = kTileRows / RPW;   // 8 for BN = 16, 4 for BN = 8
+  static constexpr int WARPS = kTileRows / RPW;   // 4 for BN = 16, 2 for BN = 8
   static constexpr int THREADS = WARPS * 32;
   static_assert(RPW * BN == 32 && WARPS * RPW == kTileRows, "shrink geometry");
 };

@@ -12,8 +12,8 @@
 //   sec. 4.2        UNSPLIT: S = 1, one block over the whole of K;
 //   sec. 4.3        DET_TREE: partials only, combined by reduce_tree.cu.
 //
-// Block = 16/RPW warps of RPW = 32/BN rows (8 x 2 for BN = 16, 4 x 4 for
-// BN = 8), tile = up to 16 token rows of one adapter (one entry of the token
+// Block = 8/RPW warps of RPW = 32/BN rows (4 x 2 for BN = 16, 2 x 4 for
+// BN = 8), tile = up to 8 token rows of one adapter (one entry of the token
 // map's tile table) x BN rank columns, one K partition. The partition
 // is streamed through shared memory in k-blocks of 256 elements by TMA
 // copies (one tiled copy for the A block, one row gather per 4 token rows,
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   const int sl = (int)(bid % p.slices);
   const int64_t t = bid / p.slices;
 
-  // Tile entry: [g, nrows, 0, 0, rows[16]]; complete before this kernel began.
+  // Tile entry: [g, nrows, consecutive, 0, rows[8]]; complete before this kernel began.
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
   if (tid == 0) {
     for (int i = 0; i < kShrinkStages; ++i) mbar_init(&bars[i], 1);
