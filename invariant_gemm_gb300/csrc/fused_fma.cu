@@ -10,9 +10,9 @@
 // integer counter, and they run the expand as a separate kernel; they name
 // the extra launch as the cost of the earlier two-kernel design (sec. 4.3)
 // and leave the expand to vLLM (Eq. 1). On GB300 the S blocks of a tile can
-// be one cluster: each block keeps its partial in its own shared memory, a
-// cluster barrier publishes them, and every block reads all S partials over
-// distributed shared memory in the same fixed order. No scratch, no
+// be one cluster: each block stores its partial into every block's shared
+// memory (distributed shared memory), one cluster barrier publishes them,
+// and every block sums the S partials in the same fixed order. No scratch, no
 // counter, and the expand of the tile's rows follows in the same launch,
 // each block taking 1/S of the output columns.
 //
@@ -43,20 +43,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Plain (non-volatile) so that the S loads of one output can be in flight
-// together; the cluster barrier before them orders them after the writes.
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+// Store into the same offset of block `rank`'s shared memory.
+__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
   uint32_t remote;
-  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
-  return v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 struct FusedLayout {
@@ -78,7 +70,7 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   L.cols = (int)(((N + S - 1) / S + 7) / 8 * 8);
   L.ring_off = 256;
   L.part_off = L.ring_off + (size_t)L.nst * PartialRing<BN>::kStageBytes;
-  L.zs_off = L.part_off + kTileRows * BN * 4;
+  L.zs_off = L.part_off + (size_t)S * kTileRows * BN * 4;
   L.b_off = L.zs_off + kTileRows * ZsStride<BN>::v * 4;
   L.bytes = L.b_off + (size_t)L.cols * BN * 2;
   return L;
@@ -94,7 +86,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // ring bars [0, 4)
   uint64_t* bar_by = bars + kShrinkStages;                       // B and y copies
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);        // tile entry
-  float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [16][BN]
+  float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [S][rows][BN]
   float* zs = reinterpret_cast<float*>(smem + lay.zs_off);       // [16][BN + 4]
   uint8_t* sB = smem + lay.b_off;                                // [cols][BN] bf16
 
@@ -200,28 +192,29 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     }
   }
 
+  // This block's partial P_s goes to slot s of every block of the cluster
+  // (its own included), so that after one cluster barrier each block sums
+  // the S partials from its own shared memory.
   float v;
   const bool ok = ring.run(pa, v);
-  part[(warp * RPW + lane / BN) * BN + lane % BN] = ok ? v : 0.0f;
+  {
+    constexpr int TB = kTileRows * BN;
+    const int o = (warp * RPW + lane / BN) * BN + lane % BN;
+    for (int q = 0; q < S; ++q) st_dsmem_f32(part + s * TB + o, (uint32_t)q, ok ? v : 0.0f);
+  }
 
-  // Every block of the cluster reaches both cluster barriers on every path.
-  cluster_sync();  // all partials written and visible across the cluster
+  // Every block of the cluster reaches the cluster barrier on every path;
+  // after it no block touches another block's shared memory.
+  cluster_sync();
 
   // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
   for (int o = tid; o < nrows * BN; o += kThreads) {
-    float pv[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-      if (q < S) pv[q] = ld_dsmem_f32(part + o, (uint32_t)q);
     float total = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-      if (q < S) total += pv[q];
+    for (int q = 0; q < S; ++q) total += part[q * kTileRows * BN + o];
     const float zv = total * p.scale;
     zs[(o / BN) * ZS + o % BN] = (p.flags & IG_FLAG_Z_FP32) ? zv : bf16_round_f32(zv);
     if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
   }
-  cluster_arrive();  // done reading the other blocks' partials
   __syncthreads();   // zs complete
 
   // Expand this block's columns: y = bf16_rn(f32(y) + sum_j zb_j B_nj), the
@@ -310,7 +303,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   // a copy that never completed: wait for it once more (bounded) before the
   // block's shared memory goes away
   if (!copies_ok) mbar_wait_bounded(bar_by, 0, p.status);
-  cluster_wait();  // no block leaves while another may still read its partial
 }
 
 }  // namespace
