@@ -21,7 +21,7 @@
 // same code (shrink_core.cuh), the combine adds them in the same order, and
 // the expand keeps the same j order and single rounding.
 //
-// Block = 8/RPW warps of RPW = 32/r rows; cluster = S blocks (rank s = K
+// Block = r/4 warps; cluster = S blocks (rank s = K
 // partition s); tile = up to 8 token rows of one adapter (tile-table entry)
 // x all r rank columns (r = 8 or 16). Copies: the A block of each k-block by
 // one tiled TMA copy, the token rows of x by row-gather TMA copies (4 rows
@@ -80,7 +80,6 @@ template <int BN>
 __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     fused_fma_kernel(const __grid_constant__ FusedParams p) {
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
-  constexpr int RPW = ShrinkGeo<BN>::RPW;
   extern __shared__ __align__(1024) uint8_t smem[];
   const FusedLayout lay = fused_layout<BN>(p.Ks, p.N, p.S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // ring bars [0, 4)
@@ -199,7 +198,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   const bool ok = ring.run(pa, v);
   {
     constexpr int TB = kTileRows * BN;
-    const int o = (warp * RPW + lane / BN) * BN + lane % BN;
+    const int o = (lane / 4) * BN + warp * ShrinkGeo<BN>::JPW + lane % 4;
     for (int q = 0; q < S; ++q) st_dsmem_f32(part + s * TB + o, (uint32_t)q, ok ? v : 0.0f);
   }
 

@@ -3,8 +3,9 @@
 // compute bit-identical partials.
 //
 // Tile: up to 8 token rows x BN rank columns (BN = 8 or 16). The block has
-// 8/RPW warps of RPW = 32/BN rows each, so every lane ends with exactly one
-// finished output. The partition [k0, k0 + Ks) is streamed through a ring of
+// BN/4 warps; warp w computes rank columns 4w .. 4w+3 for all 8 rows (32
+// outputs), so every lane ends with exactly one finished output and every
+// warp has work however few rows the tile holds. The partition [k0, k0 + Ks) is streamed through a ring of
 // `nst` shared-memory stages, k-blocks of 256 elements, completion counted in
 // bytes on one mbarrier per stage; warp 0 issues the copies. Two ways to
 // copy: with tensor maps, one tiled TMA copy brings the A block (BN rows)
@@ -28,10 +29,10 @@ namespace ig {
 
 template <int BN>
 struct ShrinkGeo {
-  static constexpr int RPW = 32 / BN;             // rows per warp
-  static constexpr int WARPS = kTileRows / RPW;   // 4 for BN = 16, 2 for BN = 8
+  static constexpr int JPW = 4;                   // rank columns per warp
+  static constexpr int WARPS = BN / JPW;          // 4 for BN = 16, 2 for BN = 8
   static constexpr int THREADS = WARPS * 32;
-  static_assert(RPW * BN == 32 && WARPS * RPW == kTileRows, "shrink geometry");
+  static_assert(kTileRows * JPW == 32 && WARPS * JPW == BN, "shrink geometry");
 };
 
 struct PartialArgs {
@@ -104,18 +105,15 @@ struct PartialRing {
   }
 
   // All threads. The first min(nkb, nst) k-blocks must already be armed and
-  // issued. On return `out` is this lane's output: row warp*RPW + lane/BN,
-  // column lane % BN (not yet scaled). Returns false if a copy wait expired
+  // issued. On return `out` is this lane's output: row lane/4, column
+  // 4*warp + lane%4 (not yet scaled). Returns false if a copy wait expired
   // (after draining, bounded, every copy still in flight).
   __device__ __forceinline__ bool run(const PartialArgs& a, float& out) const {
-    constexpr int RPW = G::RPW;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = warp * RPW;
-    float2 acc[RPW][BN / 2];
+    const int j0 = warp * G::JPW;
+    float2 acc[kTileRows][2];   // [row][column pair]
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr)
-#pragma unroll
-      for (int jp = 0; jp < BN / 2; ++jp) acc[rr][jp] = make_float2(0.0f, 0.0f);
+    for (int rr = 0; rr < kTileRows; ++rr) acc[rr][0] = acc[rr][1] = make_float2(0.0f, 0.0f);
 
     int issued = min(nkb, nst);
     int fail_b = -1;
@@ -125,35 +123,31 @@ struct PartialRing {
       const bool ok = mbar_wait_bounded(&bars[st], parity, a.status);
       if (__syncthreads_or(!ok)) { fail_b = b; break; }
       const int64_t klen = min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB);
-      if ((int64_t)lane * 8 < klen && row0 < a.nrows) {
+      if ((int64_t)lane * 8 < klen) {
         const uint8_t* sx = stages + st * kStageBytes;
         const uint8_t* sa = sx + kTileRows * kRowBytes;
-        float2 xx[RPW][8];  // each x value duplicated into both halves
+        float2 aa[2][8];   // columns (j0, j0+1) and (j0+2, j0+3), element e
 #pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-          float xv[8];
-          if (row0 + rr < a.nrows) {
-            const uint4 u = *reinterpret_cast<const uint4*>(sx + (row0 + rr) * kRowBytes + lane * 16);
-            unpack8(u, xv);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) xx[rr][e] = make_float2(xv[e], xv[e]);
-        }
-#pragma unroll
-        for (int jp = 0; jp < BN / 2; ++jp) {
-          const uint4 u0 = *reinterpret_cast<const uint4*>(sa + (2 * jp) * kRowBytes + lane * 16);
-          const uint4 u1 = *reinterpret_cast<const uint4*>(sa + (2 * jp + 1) * kRowBytes + lane * 16);
+        for (int jp = 0; jp < 2; ++jp) {
+          const uint4 u0 = *reinterpret_cast<const uint4*>(sa + (j0 + 2 * jp) * kRowBytes + lane * 16);
+          const uint4 u1 = *reinterpret_cast<const uint4*>(sa + (j0 + 2 * jp + 1) * kRowBytes + lane * 16);
           float a0[8], a1[8];
           unpack8(u0, a0);
           unpack8(u1, a1);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 aa = make_float2(a0[e], a1[e]);
+          for (int e = 0; e < 8; ++e) aa[jp][e] = make_float2(a0[e], a1[e]);
+        }
 #pragma unroll
-            for (int rr = 0; rr < RPW; ++rr) acc[rr][jp] = __ffma2_rn(xx[rr][e], aa, acc[rr][jp]);
+        for (int rr = 0; rr < kTileRows; ++rr) {
+          if (rr >= a.nrows) break;
+          const uint4 u = *reinterpret_cast<const uint4*>(sx + rr * kRowBytes + lane * 16);
+          float xv[8];
+          unpack8(u, xv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 xx = make_float2(xv[e], xv[e]);
+            acc[rr][0] = __ffma2_rn(xx, aa[0][e], acc[rr][0]);
+            acc[rr][1] = __ffma2_rn(xx, aa[1][e], acc[rr][1]);
           }
         }
       }
@@ -175,15 +169,15 @@ struct PartialRing {
       return false;
     }
 
-    // Reduce-scatter: 32 values per lane (row-major rr*BN + j) -> one per lane.
+    // Reduce-scatter: 32 values per lane (row-major rr*4 + j) -> one per lane.
     float v[32];
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr)
-#pragma unroll
-      for (int jp = 0; jp < BN / 2; ++jp) {
-        v[rr * BN + 2 * jp] = acc[rr][jp].x;
-        v[rr * BN + 2 * jp + 1] = acc[rr][jp].y;
-      }
+    for (int rr = 0; rr < kTileRows; ++rr) {
+      v[rr * 4 + 0] = acc[rr][0].x;
+      v[rr * 4 + 1] = acc[rr][0].y;
+      v[rr * 4 + 2] = acc[rr][1].x;
+      v[rr * 4 + 3] = acc[rr][1].y;
+    }
 #pragma unroll
     for (int lvl = 0; lvl < 5; ++lvl) {
       const int off = 16 >> lvl;

@@ -12,8 +12,8 @@
 //   sec. 4.2        UNSPLIT: S = 1, one block over the whole of K;
 //   sec. 4.3        DET_TREE: partials only, combined by reduce_tree.cu.
 //
-// Block = 8/RPW warps of RPW = 32/BN rows (4 x 2 for BN = 16, 2 x 4 for
-// BN = 8), tile = up to 8 token rows of one adapter (one entry of the token
+// Block = BN/4 warps (warp w: rank columns 4w .. 4w+3 of all rows), tile =
+// up to 8 token rows of one adapter (one entry of the token
 // map's tile table) x BN rank columns, one K partition. The partition
 // is streamed through shared memory in k-blocks of 256 elements by TMA
 // copies (one tiled copy for the A block, one row gather per 4 token rows,
@@ -47,7 +47,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     shrink_fma_kernel(const __grid_constant__ ShrinkParams p) {
   using SM = ShrinkSmem<BN>;
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
-  constexpr int RPW = ShrinkGeo<BN>::RPW;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);    // tile entry (kTileInts)
@@ -131,8 +130,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
 
   float v;
   if (!ring.run(pa, v)) return;
-  const int rrow = warp * RPW + lane / BN;  // this lane's output
-  const int j0 = lane % BN;
+  const int rrow = lane / 4;                 // this lane's output
+  const int j0 = warp * ShrinkGeo<BN>::JPW + lane % 4;
 
   if (MODE == IG_MODE_UNSPLIT || MODE == IG_MODE_ATOMIC) {
     if (rrow < nrows) {
