@@ -256,6 +256,12 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kShrinkKB, (uint32_t)sh->r,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != IG_OK) return rc;
+  // B as rows of 64 elements (64 / r output columns x r ranks), 128-byte
+  // swizzled boxes of b_box_rows rows
+  p.b_box_rows = fused_b_box_rows(pl.bn, pl.Ks, sh->N, pl.S);
+  rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N * sh->r / 64,
+                     64, 128, 64, (uint32_t)p.b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.A = static_cast<const __nv_bfloat16*>(A);
   p.B = static_cast<const __nv_bfloat16*>(B);

@@ -10,24 +10,30 @@
 // integer counter, and they run the expand as a separate kernel; they name
 // the extra launch as the cost of the earlier two-kernel design (sec. 4.3)
 // and leave the expand to vLLM (Eq. 1). On GB300 the S blocks of a tile can
-// be one cluster: each block stores its partial into every block's shared
-// memory (distributed shared memory), one cluster barrier publishes them,
-// and every block sums the S partials in the same fixed order. No scratch, no
-// counter, and the expand of the tile's rows follows in the same launch,
-// each block taking 1/S of the output columns.
+// be one cluster: each block sends its partial into slot s of every block's
+// shared memory with asynchronous remote stores that count their bytes on
+// the receiving block's mbarrier, so a block starts its combine as soon as
+// the S partials have landed in its own shared memory, with no cluster-wide
+// barrier on the way. Every block then sums the S partials in the same fixed
+// order. No scratch, no counter, and the expand of the tile's rows follows
+// in the same launch, each block taking 1/S of the output columns.
 //
 // Bit-for-bit the same results as the two-kernel path (shrink kernel with
 // the counter protocol, then the expand kernel): the partials come from the
 // same code (shrink_core.cuh), the combine adds them in the same order, and
 // the expand keeps the same j order and single rounding.
 //
-// Block = r/4 warps; cluster = S blocks (rank s = K
-// partition s); tile = up to 8 token rows of one adapter (tile-table entry)
-// x all r rank columns (r = 8 or 16). Copies: the A block of each k-block by
-// one tiled TMA copy, the token rows of x by row-gather TMA copies (4 rows
-// each), the block's B column slice (contiguous in B_stack) by one bulk copy;
-// the y values a thread will update are loaded into registers right after
-// griddep_wait, so they arrive while the shrink computes.
+// Block = r/4 warps; cluster = S blocks (rank s = K partition s); tile = up
+// to 8 token rows of one adapter (tile-table entry) x all r rank columns
+// (r = 8 or 16). Copies: the A block of each k-block by one tiled TMA copy,
+// the token rows of x by row-gather TMA copies (4 rows each), the block's B
+// column slice by tiled TMA copies of 128-byte rows (64/r columns x r ranks
+// each, 128-byte swizzled so that the rows read by 8 neighbouring lanes sit
+// in 8 distinct bank groups); the y values of a thread's first expand unit
+// are loaded into registers right after griddep_wait, so they arrive while
+// the shrink computes.
+#include <type_traits>
+
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -39,40 +45,63 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Split cluster barrier. The arrive carries no memory ordering: it only
+// tells the other blocks that this block's mbarriers are initialised (made
+// visible to the cluster by fence.mbarrier_init before it).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-// Store into the same offset of block `rank`'s shared memory.
-__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(const void* local, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+  return remote;
 }
+// Asynchronous 4-byte store into another block's shared memory; its bytes
+// are counted (complete_tx) on that block's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(remote), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+template <int BN>
+struct FusedGeo {
+  static constexpr int CU = 64 / BN;   // output columns per expand unit (128 bytes of B)
+  static constexpr int CP = CU / 2;    // column pairs per unit
+  static constexpr int TB = kTileRows * BN;   // partial values per block
+};
 
 struct FusedLayout {
   int nst;           // ring depth
   int cols;          // output columns per block (multiple of 8)
-  size_t ring_off, part_off, zs_off, b_off, bytes;
-};
-
-template <int BN>
-struct ZsStride {
-  static constexpr int v = BN + 4;  // padded row: 8 rows hit 8 distinct bank groups
+  int units;         // expand units per block (cols / CU), one 128-byte B row each
+  int box_rows;      // B rows per TMA box (<= 256)
+  int nbox;          // B boxes per block
+  size_t ring_off, part_off, zd_off, b_off, bytes;   // from the 1024-aligned base
 };
 
 template <int BN>
 __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S) {
+  using F = FusedGeo<BN>;
   FusedLayout L;
   const int nkb = (int)((Ks + kShrinkKB - 1) / kShrinkKB);
   L.nst = nkb < kShrinkStages ? nkb : kShrinkStages;
   L.cols = (int)(((N + S - 1) / S + 7) / 8 * 8);
+  L.units = L.cols / F::CU;
+  L.box_rows = L.units < 256 ? L.units : 256;
+  L.nbox = (L.units + L.box_rows - 1) / L.box_rows;
   L.ring_off = 256;
   L.part_off = L.ring_off + (size_t)L.nst * PartialRing<BN>::kStageBytes;
-  L.zs_off = L.part_off + (size_t)S * kTileRows * BN * 4;
-  L.b_off = L.zs_off + kTileRows * ZsStride<BN>::v * 4;
-  L.bytes = L.b_off + (size_t)L.cols * BN * 2;
+  L.zd_off = L.part_off + (size_t)S * F::TB * 4;
+  L.b_off = (L.zd_off + (size_t)F::TB * 8 + 1023) / 1024 * 1024;
+  L.bytes = L.b_off + (size_t)L.nbox * L.box_rows * 128;
   return L;
 }
 
@@ -80,14 +109,20 @@ template <int BN>
 __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     fused_fma_kernel(const __grid_constant__ FusedParams p) {
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  using F = FusedGeo<BN>;
+  constexpr int CU = F::CU, CP = F::CP, TB = F::TB;
+  using YV = typename std::conditional<CU == 4, uint2, uint4>::type;   // CU bf16 of y
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const FusedLayout lay = fused_layout<BN>(p.Ks, p.N, p.S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // ring bars [0, 4)
-  uint64_t* bar_by = bars + kShrinkStages;                       // B and y copies
+  uint64_t* bar_b = bars + kShrinkStages;                        // B copies
+  uint64_t* bar_part = bars + kShrinkStages + 1;                 // incoming partials
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);        // tile entry
-  float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [S][rows][BN]
-  float* zs = reinterpret_cast<float*>(smem + lay.zs_off);       // [16][BN + 4]
-  uint8_t* sB = smem + lay.b_off;                                // [cols][BN] bf16
+  float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [S][8][BN]
+  float2* zd = reinterpret_cast<float2*>(smem + lay.zd_off);     // [8][BN] (z, z)
+  uint8_t* sB = smem + lay.b_off;                                // [units][128 B], swizzled
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
@@ -98,9 +133,14 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
 
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
   if (tid == 0) {
+    prefetch_tensormap(&p.tm_x);
+    prefetch_tensormap(&p.tm_a);
+    prefetch_tensormap(&p.tm_b);
     for (int i = 0; i < lay.nst; ++i) mbar_init(&bars[i], 1);
-    mbar_init(bar_by, 1);
+    mbar_init(bar_b, 1);
+    mbar_init(bar_part, 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(bar_part, (uint32_t)(S * TB * 4));
   }
   __syncthreads();
   const int g = ent_s[0];
@@ -119,12 +159,14 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
         p.z[((int64_t)sl * M + rows_s[i / r]) * r + i % r] = 0.0f;
     return;
   }
+  // every block of the cluster has initialised and armed its mbarriers once
+  // the matching cluster_wait returns
+  cluster_arrive_relaxed();
 
   // this block's output columns [c0, c0 + ncols) of slice sl
   const int64_t c0 = (int64_t)s * lay.cols;
   const int ncols = (int)max((int64_t)0, min((int64_t)lay.cols, N - c0));
-  const int groups = ncols / 8;
-  constexpr int ZS = ZsStride<BN>::v;
+  const int nunits = ncols / CU;
   const bool early_w = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
 
   PartialArgs pa;
@@ -146,18 +188,25 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   ring.nkb = (int)((p.Ks + kShrinkKB - 1) / kShrinkKB);
   const int first = min(ring.nkb, lay.nst);
 
-  const __nv_bfloat16* Bsrc = p.B + (((int64_t)g * p.slices + sl) * N + c0) * r;
-  const uint32_t b_bytes = (uint32_t)ncols * r * 2;
+  // B rows of this block: 128-byte row u holds columns c0 + CU*u .. + CU-1
+  const int b_row0 = (int)((((int64_t)g * p.slices + sl) * N + c0) / CU);
+  auto issue_b = [&]() {
+    if (lane == 0 && ncols > 0)
+      for (int bi = 0; bi < lay.nbox; ++bi)
+        tma_load_2d(sB + (size_t)bi * lay.box_rows * 128, &p.tm_b, 0,
+                    b_row0 + bi * lay.box_rows, bar_b);
+  };
   const int64_t ldy = (int64_t)p.slices * N;
 
   if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(bar_by, b_bytes);
+    if (lane == 0)
+      mbar_arrive_expect_tx(bar_b, ncols > 0 ? (uint32_t)(lay.nbox * lay.box_rows * 128) : 0u);
     __syncwarp();
     for (int b = 0; b < first; ++b) {
       ring.expect(pa, b);
       if (early_w) ring.issue_a(pa, b);
     }
-    if (early_w && lane == 0 && b_bytes) bulk_g2s(sB, Bsrc, b_bytes, bar_by);
+    if (early_w) issue_b();
   }
   griddep_wait();
   griddep_launch();
@@ -166,148 +215,117 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
       if (!early_w) ring.issue_a(pa, b);
       ring.issue_x(pa, b);
     }
-    if (!early_w && lane == 0 && b_bytes) bulk_g2s(sB, Bsrc, b_bytes, bar_by);
+    if (!early_w) issue_b();
   }
 
-  // Expand work units: (pair of rows rp, 8-column group q), rp varying
-  // fastest so that the 8 lanes of a shared-memory phase read the same B
-  // group (broadcast) and rows of Z that sit in distinct banks. The y values
-  // of a thread's first two units are loaded now and arrive during the
-  // shrink.
-  const int pairs = (nrows + 1) / 2;
-  const int units = pairs * groups;
-  uint4 ypre[2][2];
+  // y of the thread's first expand unit (all tile rows), loaded now so that
+  // it arrives during the shrink
+  YV ypre[kTileRows];
+  if (tid < nunits) {
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int u = tid + k * kThreads;
-    if (u < units) {
-      const int rp = u % pairs, q = u / pairs;
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int row = min(2 * rp + i, nrows - 1);
-        ypre[k][i] = *reinterpret_cast<const uint4*>(p.y + (int64_t)rows_s[row] * ldy +
-                                                     (int64_t)sl * N + c0 + q * 8);
-      }
-    }
+    for (int rr = 0; rr < kTileRows; ++rr)
+      if (rr < nrows)
+        ypre[rr] = *reinterpret_cast<const YV*>(p.y + (int64_t)rows_s[rr] * ldy +
+                                                (int64_t)sl * N + c0 + CU * tid);
   }
 
-  // This block's partial P_s goes to slot s of every block of the cluster
-  // (its own included), so that after one cluster barrier each block sums
-  // the S partials from its own shared memory.
   float v;
   const bool ok = ring.run(pa, v);
-  {
-    constexpr int TB = kTileRows * BN;
-    const int o = (lane / 4) * BN + warp * ShrinkGeo<BN>::JPW + lane % 4;
-    for (int q = 0; q < S; ++q) st_dsmem_f32(part + s * TB + o, (uint32_t)q, ok ? v : 0.0f);
-  }
 
-  // Every block of the cluster reaches the cluster barrier on every path;
-  // after it no block touches another block's shared memory.
-  cluster_sync();
+  // Send this block's partial P_s to slot s of every block of the cluster
+  // (its own included). Every block sends on every path (zeros after a
+  // failed copy), so every block receives exactly S * TB * 4 bytes.
+  cluster_wait();
+  {
+    const int o = (lane / 4) * BN + warp * ShrinkGeo<BN>::JPW + lane % 4;
+    const float pv = ok ? v : 0.0f;
+    for (int q = 0; q < S; ++q)
+      st_async_f32(map_rank(part + s * TB + o, (uint32_t)q), pv, map_rank(bar_part, (uint32_t)q));
+  }
+  // The wait outlasts any sender's own bounded waits, so a block never
+  // leaves while a partial is still on its way to it.
+  const bool got = mbar_wait_bounded(bar_part, 0, p.status, 1ll << 36);
 
   // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
   for (int o = tid; o < nrows * BN; o += kThreads) {
     float total = 0.0f;
-    for (int q = 0; q < S; ++q) total += part[q * kTileRows * BN + o];
+    for (int q = 0; q < S; ++q) total += part[q * TB + o];
     const float zv = total * p.scale;
-    zs[(o / BN) * ZS + o % BN] = (p.flags & IG_FLAG_Z_FP32) ? zv : bf16_round_f32(zv);
+    const float zb = (p.flags & IG_FLAG_Z_FP32) ? zv : bf16_round_f32(zv);
+    zd[o] = make_float2(zb, zb);
     if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
   }
-  __syncthreads();   // zs complete
+  __syncthreads();   // zd complete
 
   // Expand this block's columns: y = bf16_rn(f32(y) + sum_j zb_j B_nj), the
-  // j sum a chain of FMAs in increasing j (two columns per f32x2 FMA). Work
-  // units are (pair of rows, 8-column group), spread over all threads of
-  // the block; every element is computed by one thread, so the split does
-  // not change any result.
-  const bool copies_ok = mbar_wait_bounded(bar_by, 0, p.status);
-  if (copies_ok) {
-    for (int k = 0; tid + k * kThreads < units; ++k) {
-      const int u = tid + k * kThreads;
-      const int rp = u % pairs, q = u / pairs;
-      const int ra = 2 * rp, rb = 2 * rp + 1;
-      const bool has_b = rb < nrows;
-      uint4 yv[2];
-      if (k == 0) {
-        yv[0] = ypre[0][0];
-        yv[1] = ypre[0][1];
-      } else if (k == 1) {
-        yv[0] = ypre[1][0];
-        yv[1] = ypre[1][1];
-      } else {
+  // j sum a chain of FMAs in increasing j (two columns per f32x2 FMA). A unit
+  // is CU consecutive columns for all rows of the tile: its B values are
+  // converted once and used for every row. Every element is computed by one
+  // thread, so the split does not change any result.
+  const bool copies_ok = mbar_wait_bounded(bar_b, 0, p.status);
+  if (copies_ok && got) {
+    for (int u = tid, k = 0; u < nunits; u += kThreads, ++k) {
+      float2 bp[CP][BN];   // (B[c][j], B[c+1][j]) for column pair c = 2cp
+      {
+        const uint8_t* row = sB + (size_t)u * 128;
+        const int sw = u & 7;   // 128-byte swizzle: 16-byte chunk i sits at i ^ (row % 8)
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-          yv[i] = *reinterpret_cast<const uint4*>(p.y + (int64_t)rows_s[min(ra + i, nrows - 1)] *
-                                                  ldy + (int64_t)sl * N + c0 + q * 8);
-      }
-      float2 acc[2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int cp = 0; cp < 4; ++cp) acc[i][cp] = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int h = 0; h < BN / 8; ++h) {
-        float za[8], zb[8];
-        {
-          const float4 a0 = *reinterpret_cast<const float4*>(zs + ra * ZS + 8 * h);
-          const float4 a1 = *reinterpret_cast<const float4*>(zs + ra * ZS + 8 * h + 4);
-          const float4 b0 = *reinterpret_cast<const float4*>(zs + (has_b ? rb : ra) * ZS + 8 * h);
-          const float4 b1 =
-              *reinterpret_cast<const float4*>(zs + (has_b ? rb : ra) * ZS + 8 * h + 4);
-          za[0] = a0.x; za[1] = a0.y; za[2] = a0.z; za[3] = a0.w;
-          za[4] = a1.x; za[5] = a1.y; za[6] = a1.z; za[7] = a1.w;
-          zb[0] = b0.x; zb[1] = b0.y; zb[2] = b0.z; zb[3] = b0.w;
-          zb[4] = b1.x; zb[5] = b1.y; zb[6] = b1.z; zb[7] = b1.w;
-        }
-#pragma unroll
-        for (int cp = 0; cp < 4; ++cp) {
-          const uint4 u0 =
-              *reinterpret_cast<const uint4*>(sB + ((q * 8 + 2 * cp) * r + 8 * h) * 2);
-          const uint4 u1 =
-              *reinterpret_cast<const uint4*>(sB + ((q * 8 + 2 * cp + 1) * r + 8 * h) * 2);
-          float b0[8], b1[8];
-          unpack8(u0, b0);
-          unpack8(u1, b1);
+        for (int i = 0; i < 8; ++i) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + ((i ^ sw) << 4));
+          float f[8];
+          unpack8(w, f);
+          const int cc = (8 * i) / BN, jb = (8 * i) % BN;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float2 bb = make_float2(b0[e], b1[e]);
-            acc[0][cp] = __ffma2_rn(make_float2(za[e], za[e]), bb, acc[0][cp]);
-            acc[1][cp] = __ffma2_rn(make_float2(zb[e], zb[e]), bb, acc[1][cp]);
+            if (cc % 2 == 0) bp[cc / 2][jb + e].x = f[e];
+            else bp[cc / 2][jb + e].y = f[e];
           }
         }
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int row = ra + i;
-        if (row >= nrows) break;
-        float yf[8];
-        unpack8(yv[i], yf);
-        uint32_t o[8];
+      for (int rr = 0; rr < kTileRows; ++rr) {
+        if (rr >= nrows) break;
+        __nv_bfloat16* yp = p.y + (int64_t)rows_s[rr] * ldy + (int64_t)sl * N + c0 + CU * u;
+        const YV yv = k == 0 ? ypre[rr] : *reinterpret_cast<const YV*>(yp);
+        float2 acc[CP];
 #pragma unroll
-        for (int cp = 0; cp < 4; ++cp) {
-          o[2 * cp] = f32_to_bf16_bits(yf[2 * cp] + acc[i][cp].x);
-          o[2 * cp + 1] = f32_to_bf16_bits(yf[2 * cp + 1] + acc[i][cp].y);
+        for (int cp = 0; cp < CP; ++cp) acc[cp] = make_float2(0.0f, 0.0f);
+        const float4* zr = reinterpret_cast<const float4*>(zd + rr * BN);
+#pragma unroll
+        for (int jj = 0; jj < BN / 2; ++jj) {
+          const float4 z2 = zr[jj];   // (z_j, z_j, z_j+1, z_j+1)
+#pragma unroll
+          for (int cp = 0; cp < CP; ++cp)
+            acc[cp] = __ffma2_rn(make_float2(z2.x, z2.y), bp[cp][2 * jj], acc[cp]);
+#pragma unroll
+          for (int cp = 0; cp < CP; ++cp)
+            acc[cp] = __ffma2_rn(make_float2(z2.z, z2.w), bp[cp][2 * jj + 1], acc[cp]);
         }
-        uint4 w;
-        w.x = o[0] | (o[1] << 16);
-        w.y = o[2] | (o[3] << 16);
-        w.z = o[4] | (o[5] << 16);
-        w.w = o[6] | (o[7] << 16);
-        *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[row] * ldy + (int64_t)sl * N + c0 +
-                                  q * 8) = w;
+        const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
+        YV out;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+        for (int cp = 0; cp < CP; ++cp)
+          ow[cp] = f32_to_bf16_bits(bf16lo(yw[cp]) + acc[cp].x) |
+                   (f32_to_bf16_bits(bf16hi(yw[cp]) + acc[cp].y) << 16);
+        *reinterpret_cast<YV*>(yp) = out;
       }
     }
   }
   // a copy that never completed: wait for it once more (bounded) before the
   // block's shared memory goes away
-  if (!copies_ok) mbar_wait_bounded(bar_by, 0, p.status);
+  if (!copies_ok) mbar_wait_bounded(bar_b, 0, p.status);
 }
 
 }  // namespace
 
 size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S) {
-  return bn == 16 ? fused_layout<16>(Ks, N, S).bytes : fused_layout<8>(Ks, N, S).bytes;
+  // + 1024: the kernel aligns its base to 1024 bytes (128-byte swizzle atoms)
+  return 1024 + (bn == 16 ? fused_layout<16>(Ks, N, S).bytes : fused_layout<8>(Ks, N, S).bytes);
+}
+
+int fused_b_box_rows(int bn, int64_t Ks, int64_t N, int S) {
+  return bn == 16 ? fused_layout<16>(Ks, N, S).box_rows : fused_layout<8>(Ks, N, S).box_rows;
 }
 
 cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st) {

@@ -113,6 +113,8 @@ int encode_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t co
 struct FusedParams {
   CUtensorMap tm_x;     // x [M][K], box 256 x 1 (row gathers)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 256 x r
+  CUtensorMap tm_b;     // B_stack as rows of 64 elements (64/r output columns
+                        // x r), box 64 x b_box_rows, 128-byte swizzle
   const __nv_bfloat16* x;
   const __nv_bfloat16* A;
   const __nv_bfloat16* B;
@@ -122,6 +124,7 @@ struct FusedParams {
   uint32_t* status;
   int64_t M, K, N, Ks;
   int32_t slices, L, S, flags;
+  int32_t b_box_rows;
   float scale;
 };
 
@@ -168,6 +171,7 @@ cudaError_t launch_expand_fma(const ExpandParams& p, int64_t tiles_max,
                               cudaStream_t st);
 cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st);
 size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S);
+int fused_b_box_rows(int bn, int64_t Ks, int64_t N, int S);
 cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
                               cudaStream_t st);
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st);
@@ -256,11 +260,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on an mbarrier phase. Gives up after ~2^31 SM clocks (about a
 // second), records kStatusTimeout and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t* status) {
+                                                  uint32_t* status,
+                                                  long long budget = 1ll << 31) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (1ll << 31)) {
+    if (clock64() - t0 > budget) {
       atomicOr(status, kStatusTimeout);
       return false;
     }

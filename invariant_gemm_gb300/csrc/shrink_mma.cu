@@ -247,20 +247,41 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     if ((uint32_t)ctl->info[0] == (uint32_t)(S - 1)) {
       __threadfence();
-      // four consecutive columns of one row per step (r is a multiple of 16)
-      for (int o = 4 * tid; o < nrows * r; o += 4 * kThreads) {
-        float4 total = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      // Each thread owns up to 16 float4 outputs (four consecutive columns of
+      // one row) and adds the partitions q = 0..S-1 in order; the 16 loads of
+      // one partition are in flight together.
+      constexpr int kPer = 16;
+      const int n4 = nrows * r / 4;
+      for (int base = 0; base < n4; base += kPer * kThreads) {
+        float4 tot[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) tot[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         for (int q = 0; q < S; ++q) {
-          const float4 v =
-              __ldcg(reinterpret_cast<const float4*>(part + (int64_t)q * (kMmaTileRows * r) + o));
-          total.x += v.x;
-          total.y += v.y;
-          total.z += v.z;
-          total.w += v.w;
+          const float4* src =
+              reinterpret_cast<const float4*>(part + (int64_t)q * (kMmaTileRows * r));
+          float4 v[kPer];
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int o4 = base + i * kThreads + tid;
+            v[i] = o4 < n4 ? __ldcg(src + o4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          }
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            tot[i].x += v[i].x;
+            tot[i].y += v[i].y;
+            tot[i].z += v[i].z;
+            tot[i].w += v[i].w;
+          }
         }
-        *reinterpret_cast<float4*>(p.z + ((int64_t)sl * M + rows_s[o / r]) * r + o % r) =
-            make_float4(total.x * p.scale, total.y * p.scale, total.z * p.scale,
-                        total.w * p.scale);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int o4 = base + i * kThreads + tid;
+          if (o4 >= n4) continue;
+          const int o = 4 * o4;
+          *reinterpret_cast<float4*>(p.z + ((int64_t)sl * M + rows_s[o / r]) * r + o % r) =
+              make_float4(tot[i].x * p.scale, tot[i].y * p.scale, tot[i].z * p.scale,
+                          tot[i].w * p.scale);
+        }
       }
       if (tid == 0) p.counters[slot] = 0u;
     }
