@@ -322,7 +322,7 @@ def prefill_bench(ig, device, steps):
         u = int(torch.unique(probs[0].idx).numel())
         b = alg_bytes(M, K, N, r, sl, u)
         flops = 2 * M * K * r * sl + 2 * M * r * N * sl
-        res = {"path": "tcgen05" if info["path"] == ig.PATH_MMA else "fma"}
+        res = {"path": "tcgen05" if info["path"] == ig.PATH_MMA else "warp"}
         for part in ("apply", "shrink", "expand"):
             def body(stream, part=part):
                 for p in probs:
@@ -403,9 +403,9 @@ def atomic_replay_stats(ig, st, n):
 
 
 KERNEL_SOURCES = {
-    "fused_fma.cu": ["fused_fma.cu", "shrink_core.cuh", "ig_common.cuh"],
-    "shrink_fma.cu": ["shrink_fma.cu", "shrink_core.cuh", "ig_common.cuh"],
-    "expand_fma.cu": ["expand_fma.cu", "ig_common.cuh"],
+    "fused_warp.cu": ["fused_warp.cu", "shrink_core.cuh", "warp_mma.cuh", "ig_common.cuh"],
+    "shrink_warp.cu": ["shrink_warp.cu", "shrink_core.cuh", "warp_mma.cuh", "ig_common.cuh"],
+    "expand_warp.cu": ["expand_warp.cu", "warp_mma.cuh", "ig_common.cuh"],
 }
 
 
@@ -625,12 +625,12 @@ def main():
     # dominant kernel roofline: per-launch CUDA-event durations
     kd = kernel_durations(ig, st, ws[ig.MODE_DET], max(20, args.steps // 4))
     b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
-    kern = {"fused_fma (lora_apply, det)": (kd["fused"], b["total"], "fused_fma.cu"),
-            "shrink_fma (lora_shrink, det, two-kernel path)": (kd["shrink"], b["shrink"],
-                                                               "shrink_fma.cu"),
-            "expand_fma (lora_expand, two-kernel path)": (kd["expand"], b["expand"],
-                                                          "expand_fma.cu")}
-    dom = "fused_fma (lora_apply, det)"
+    kern = {"fused_warp (lora_apply, det)": (kd["fused"], b["total"], "fused_warp.cu"),
+            "shrink_warp (lora_shrink, det, two-kernel path)": (kd["shrink"], b["shrink"],
+                                                               "shrink_warp.cu"),
+            "expand_warp (lora_expand, two-kernel path)": (kd["expand"], b["expand"],
+                                                          "expand_warp.cu")}
+    dom = "fused_warp (lora_apply, det)"
     d_ms, d_bytes, d_file = kern[dom]
     achieved = d_bytes / (d_ms * 1e-3) / 1e9
     wkey = f"M={W['M']},K={W['K']},N={W['N']},r={W['r']},L={W['L']},S={W['S']}"

@@ -100,8 +100,10 @@ typedef enum ig_mode {
  * another path gives results within tolerance but not bit-equal. */
 typedef enum ig_path {
   IG_PATH_AUTO = 0,  /* chosen from (K, r, N, slices) only, never from M */
-  IG_PATH_FMA = 1,   /* CUDA-core FP32 FMA with warp-shuffle reductions */
-  IG_PATH_MMA = 2    /* tcgen05 tensor cores, FP32 accumulation in TMEM */
+  IG_PATH_WARP = 1,  /* small ranks: 8-token tiles on the warp-level tensor
+                        cores (bf16 mma.sync m16n8k16, FP32 accumulation) */
+  IG_PATH_MMA = 2    /* 128-token tiles on the tcgen05 tensor cores, FP32
+                        accumulation in TMEM */
 } ig_path;
 
 typedef struct ig_shape {
@@ -133,16 +135,18 @@ typedef struct ig_shape {
 #define IG_FLAG_Z_FP32 4         /* The expand reads Z in FP32 instead of
                                     rounding it to bf16 first (sec. 6.2 shows
                                     the bf16 boundary turning tiny FP32
-                                    differences into visible ones). CUDA-core
-                                    path: Z is used as stored. Tensor-core
-                                    path: Z = hi + lo with hi = bf16_rn(Z),
-                                    lo = bf16_rn(Z - hi), two MMAs per K step
-                                    (16 significant bits of Z). */
+                                    differences into visible ones). Warp
+                                    path: Z = hi + mid + lo exactly (three
+                                    bf16 parts, three MMAs per j chunk).
+                                    tcgen05 path: Z = hi + lo with hi =
+                                    bf16_rn(Z), lo = bf16_rn(Z - hi), two
+                                    MMAs per K step (16 significant bits of
+                                    Z). */
 
 /* The resolved plan. Everything that fixes the arithmetic is in
  * determinism_key, which never depends on M. */
 typedef struct ig_plan_info {
-  int32_t path;             /* IG_PATH_FMA or IG_PATH_MMA */
+  int32_t path;             /* IG_PATH_WARP or IG_PATH_MMA */
   int32_t split_k;          /* S used (1 for IG_MODE_UNSPLIT) */
   int64_t k_split;          /* K / S: elements per partition */
   int32_t shrink_bm;        /* shrink output tile: token rows ... */
@@ -155,7 +159,7 @@ typedef struct ig_plan_info {
   uint64_t determinism_key; /* hash of the arithmetic-defining plan fields */
   int32_t apply_kernels;    /* kernels lora_apply launches after the token
                                map: 1 = fused shrink+expand (IG_MODE_DET,
-                               r = 8 or 16, S <= 16, FMA path), 2 = shrink
+                               r = 8 or 16, S <= 16, warp path), 2 = shrink
                                then expand */
   int32_t reserved;
 } ig_plan_info;

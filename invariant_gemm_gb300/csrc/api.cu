@@ -11,7 +11,7 @@ namespace ig {
 namespace {
 
 struct Plan {
-  int path;          // IG_PATH_FMA / IG_PATH_MMA
+  int path;          // IG_PATH_WARP / IG_PATH_MMA
   int mode;
   int S;             // partitions
   int64_t Ks;        // K / S
@@ -55,7 +55,7 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   // never from M.
   const bool mma_ok = r % 16 == 0 && (K / S) % 16 == 0 && r <= 256;
   int path = sh->path;
-  if (path == IG_PATH_AUTO) path = (mma_ok && r >= 32) ? IG_PATH_MMA : IG_PATH_FMA;
+  if (path == IG_PATH_AUTO) path = (mma_ok && r >= 32) ? IG_PATH_MMA : IG_PATH_WARP;
   if (path == IG_PATH_MMA && !mma_ok) return IG_ERR_UNSUPPORTED;
 
   pl->path = path;
@@ -83,12 +83,12 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   if (partials) part = (size_t)slots * S * pl->tile_rows * pl->bn * sizeof(float);
   pl->total = align_up(pl->off_partials + part, 256);
 
-  pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_FMA && (r == 8 || r == 16) &&
+  pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_WARP && (r == 8 || r == 16) &&
               pl->bn == r && S <= 16 && !(sh->flags & IG_FLAG_UNFUSED) &&
               fused_smem_bytes(pl->bn, pl->Ks, N, S) <= 200 * 1024;
 
   uint64_t h = 1469598103934665603ull;
-  const int64_t fields[] = {IG_ABI_VERSION, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
+  const int64_t fields[] = {IG_ABI_VERSION, kArithRevision, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
                             pl->bn, mma ? 64 : kShrinkKB, sh->flags & IG_FLAG_Z_FP32};
   for (int64_t f : fields) h = fnv1a(h, f);
   pl->key = h;
@@ -219,12 +219,18 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st);
   ShrinkParams p;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+                         64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
-                     (uint64_t)sh->K, (uint64_t)sh->K * 2, kShrinkKB, (uint32_t)pl.bn,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)pl.bn,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
+  p.has_a3 = sh->K % 64 == 0 && pl.Ks % 64 == 0;
+  if (p.has_a3) {
+    rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
+                       (uint64_t)sh->K, (uint32_t)pl.bn);
+    if (rc != IG_OK) return rc;
+  }
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.A = static_cast<const __nv_bfloat16*>(A);
   p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
@@ -242,20 +248,26 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   p.jblocks = pl.jblocks;
   p.flags = sh->flags;
   p.scale = scale;
-  return cuda_status(launch_shrink_fma(p, pl.mode, pl.bn, pl.tiles, st));
+  return cuda_status(launch_shrink_warp(p, pl.mode, pl.bn, pl.tiles, st));
 }
 
 int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, const void* B,
               float scale, float* z, void* y, uint8_t* ws, cudaStream_t st) {
   FusedParams p;
-  // x rows are gathered 4 at a time (box 256 x 1); A blocks are r rows high
+  // x rows are gathered 4 at a time (box 64 x 1); A blocks are r rows high
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+                         64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
-                     (uint64_t)sh->K, (uint64_t)sh->K * 2, kShrinkKB, (uint32_t)sh->r,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)sh->r,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
+  p.has_a3 = sh->K % 64 == 0 && pl.Ks % 64 == 0;
+  if (p.has_a3) {
+    rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
+                       (uint64_t)sh->K, (uint32_t)sh->r);
+    if (rc != IG_OK) return rc;
+  }
   // B as rows of 64 elements (64 / r output columns x r ranks), 128-byte
   // swizzled boxes of b_box_rows rows
   p.b_box_rows = fused_b_box_rows(pl.bn, pl.Ks, sh->N, pl.S);
@@ -278,13 +290,17 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
   p.S = pl.S;
   p.flags = sh->flags;
   p.scale = scale;
-  return cuda_status(launch_fused_fma(p, pl.bn, pl.tiles, st));
+  return cuda_status(launch_fused_warp(p, pl.bn, pl.tiles, st));
 }
 
 int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
                uint8_t* ws, cudaStream_t st) {
   if (pl.path == IG_PATH_MMA) return run_expand_mma(sh, pl, z, B, y, ws, st);
   ExpandParams p;
+  int rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N * sh->r / 64,
+                         64, 128, 64, (uint32_t)expand_warp_box_rows((int)sh->r, sh->N),
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != IG_OK) return rc;
   p.z = z;
   p.B = static_cast<const __nv_bfloat16*>(B);
   p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
@@ -297,7 +313,7 @@ int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B
   p.L = sh->num_adapters;
   p.ntiles = pl.ntiles;
   p.flags = sh->flags;
-  return cuda_status(launch_expand_fma(p, pl.tiles, st));
+  return cuda_status(launch_expand_warp(p, pl.tiles, st));
 }
 
 }  // namespace

@@ -1,0 +1,193 @@
+// LoRA expand for small ranks: y += bf16(Z) B_i^T, in place, one rounding,
+// on the warp-level tensor cores.
+//
+// "Reproducible LoRA Inference Through Deterministic Split-K Reduction",
+// Eq. 1 (the expand multiplies the r-wide shrink output by B in
+// R^{Hout x r}) and sec. 6.2 / Fig. 5 (the FP32 shrink output reaches the
+// next operation as BF16, rounded to nearest).
+//
+// For each output element:
+//   D = tensor-core sum over j of bf16_rn(z[j]) * B[n][j]   (FP32)
+//   y = bf16_rn(f32(y) + D)
+// with the MMA sequence of warp_mma.cuh: 16-element j chunks in increasing
+// order (m16n8k16, then m16n8k8 for a last 8), D rows = the tile's token
+// rows, D columns = 8 output columns. Every element comes from one MMA of
+// one warp, so the result does not depend on the tiling, on M or on the
+// other rows, and it is the same as the fused decode kernel's.
+//
+// Block = 4 warps, tile = up to 8 token rows of one adapter (one entry of
+// the token map's tile table) x 256 output columns of one slice. The
+// block's B columns are copied by TMA as 128-byte rows (128-byte swizzle);
+// the tile's Z rows are read from global memory once, rounded (or split
+// into three bf16 parts with IG_FLAG_Z_FP32) into shared memory. Warp w
+// takes the 8-column blocks w, w+4, ...; lane 4g + t updates row g, columns
+// 2t and 2t+1 of each.
+//
+// Latency: the tile entry is read before griddep_wait(); with
+// IG_FLAG_STATIC_WEIGHTS the block's B copy is issued before it too. After
+// the wait each lane issues its y loads, then Z is read and the MMAs run.
+#include <type_traits>
+
+#include "warp_mma.cuh"
+
+namespace ig {
+
+namespace {
+
+constexpr int kThreads = kExpandWarps * 32;
+constexpr int kMaxRank = 256;
+constexpr int kPre = kExpandBN / 8 / kExpandWarps;   // y words per lane (8)
+
+struct ExpandLayout {
+  int box_rows, nbox;
+  size_t zb_off, b_off, bytes;
+};
+
+__host__ __device__ inline ExpandLayout expand_layout(int r, int64_t N) {
+  ExpandLayout L;
+  const int cols = (int)(N < kExpandBN ? N : kExpandBN);
+  const int brows = cols * r / 64;   // 128-byte B rows of a full block
+  L.box_rows = brows < 256 ? brows : 256;
+  L.nbox = (brows + L.box_rows - 1) / L.box_rows;
+  L.zb_off = 64;
+  L.b_off = (L.zb_off + (size_t)3 * kTileRows * r * 2 + 1023) / 1024 * 1024;
+  L.bytes = L.b_off + (size_t)L.nbox * L.box_rows * 128;
+  return L;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    expand_warp_kernel(const __grid_constant__ ExpandParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int r = (int)p.r;
+  const ExpandLayout lay = expand_layout(r, p.N);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+  uint16_t* zb = reinterpret_cast<uint16_t*>(smem + lay.zb_off);   // [3][8][r]
+  uint8_t* sB = smem + lay.b_off;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  int64_t bid = blockIdx.x;
+  const int nt = (int)(bid % p.ntiles);
+  bid /= p.ntiles;
+  const int sl = (int)(bid % p.slices);
+  const int64_t t = bid / p.slices;
+
+  // Tile entry [g, nrows, consecutive, 0, rows[8]]; complete before this kernel began.
+  const int32_t* ent = p.tiles + t * kTileInts;
+  const int g = ent[0];
+  const int nrows = ent[1];
+  if (g < 0 || g >= p.L || nrows <= 0) return;
+
+  const int64_t N = p.N;
+  const int64_t n0 = (int64_t)nt * kExpandBN;
+  const int ncols = (int)min((int64_t)kExpandBN, N - n0);
+  const int nblk = ncols / 8;
+  const int brows = ncols * r / 64;
+  const int nbox = (brows + lay.box_rows - 1) / lay.box_rows;
+  const bool early_b = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
+  const int b_row0 = (int)((((int64_t)g * p.slices + sl) * N + n0) * r / 64);
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, (uint32_t)(nbox * lay.box_rows * 128));
+  }
+  __syncthreads();
+  auto issue_b = [&]() {
+    if (tid == 0)
+      for (int bi = 0; bi < nbox; ++bi)
+        tma_load_2d(sB + (size_t)bi * lay.box_rows * 128, &p.tm_b, 0, b_row0 + bi * lay.box_rows,
+                    bar);
+  };
+  if (early_b) issue_b();
+
+  griddep_wait();
+  griddep_launch();
+  if (!early_b) issue_b();
+
+  const int64_t M = p.M;
+  const int gq = lane >> 2, tq = lane & 3;
+  const bool has_row = gq < nrows;
+  __nv_bfloat16* yrow = p.y + (int64_t)ent[4 + min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
+                        (int64_t)sl * N + n0 + 2 * tq;
+  uint32_t ypre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i)
+    if (has_row && warp + i * kExpandWarps < nblk)
+      ypre[i] = *reinterpret_cast<const uint32_t*>(yrow + (warp + i * kExpandWarps) * 8);
+
+  // The tile's Z rows -> bf16 parts in shared memory (rows past nrows zero).
+  // L2 only: Z was written by the previous kernel.
+  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
+  for (int o = tid; o < kTileRows * r; o += kThreads) {
+    const int row = o / r;
+    uint16_t hi = 0, mid = 0, lo = 0;
+    if (row < nrows) split_z(__ldcg(p.z + ((int64_t)sl * M + ent[4 + row]) * r + o % r), zf32,
+                             hi, mid, lo);
+    zb[o] = hi;
+    zb[kTileRows * r + o] = mid;
+    zb[2 * kTileRows * r + o] = lo;
+  }
+  __syncthreads();
+  // every thread waits for the B slice, so the block never exits with copies
+  // in flight
+  if (!mbar_wait_bounded(bar, 0, p.status)) return;
+
+  const uint32_t sB_addr = smem_u32(sB);
+  const int parts = zf32 ? 3 : 1;
+  auto store = [&](int blk, uint32_t yv, const float (&d)[4]) {
+    if (has_row)
+      *reinterpret_cast<uint32_t*>(yrow + blk * 8) =
+          f32_to_bf16_bits(bf16lo(yv) + d[0]) | (f32_to_bf16_bits(bf16hi(yv) + d[1]) << 16);
+  };
+  if (!zf32 && (r == 16 || r == 8)) {
+    // B operands of the warp's blocks, then their MMAs, then the y updates
+    // (the same MMA per block as expand_block_mma)
+    auto run = [&](auto rank) {
+      constexpr int R = decltype(rank)::value;
+      ExpandFrag<R> zf;
+      zf.load_z(zb, lane);
+      uint32_t bq[kPre][2];
+#pragma unroll
+      for (int i = 0; i < kPre; ++i)
+        ExpandFrag<R>::load_b(sB_addr, min(warp + i * kExpandWarps, nblk - 1) * 8, lane, bq[i]);
+      float dq[kPre][4];
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) zf.mma(dq[i], bq[i]);
+#pragma unroll
+      for (int i = 0; i < kPre; ++i)
+        if (warp + i * kExpandWarps < nblk) store(warp + i * kExpandWarps, ypre[i], dq[i]);
+    };
+    if (r == 16) run(std::integral_constant<int, 16>());
+    else run(std::integral_constant<int, 8>());
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int blk = warp + i * kExpandWarps;
+    if (blk >= nblk) break;
+    float d[4];
+    expand_block_mma(d, sB_addr, blk * 8, r, zb, parts, lane);
+    store(blk, ypre[i], d);
+  }
+}
+
+}  // namespace
+
+size_t expand_warp_smem_bytes(int r, int64_t N) { return 1024 + expand_layout(r, N).bytes; }
+int expand_warp_box_rows(int r, int64_t N) { return expand_layout(r, N).box_rows; }
+
+cudaError_t launch_expand_warp(const ExpandParams& p, int64_t tiles_max, cudaStream_t st) {
+  if (p.r > kMaxRank || p.r % 8 != 0) return cudaErrorInvalidValue;
+  const int64_t grid = tiles_max * p.slices * p.ntiles;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const size_t smem = expand_warp_smem_bytes((int)p.r, p.N);
+  cudaError_t e = cudaFuncSetAttribute(expand_warp_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(expand_warp_kernel, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
+}
+
+}  // namespace ig

@@ -25,15 +25,14 @@
 //
 // Block = r/4 warps; cluster = S blocks (rank s = K partition s); tile = up
 // to 8 token rows of one adapter (tile-table entry) x all r rank columns
-// (r = 8 or 16). Copies: the A block of each k-block by one tiled TMA copy,
-// the token rows of x by row-gather TMA copies (4 rows each), the block's B
-// column slice by tiled TMA copies of 128-byte rows (64/r columns x r ranks
-// each, 128-byte swizzled so that the rows read by 8 neighbouring lanes sit
-// in 8 distinct bank groups); the y values of a thread's first expand unit
-// are loaded into registers right after griddep_wait, so they arrive while
-// the shrink computes.
-#include <type_traits>
-
+// (r = 8 or 16). Copies: per 64-element sub-block the A rows by one tiled TMA
+// copy and the token rows of x by row-gather TMA copies (4 rows each); the
+// block's B column slice by tiled TMA copies of 128-byte rows (64/r columns
+// x r ranks each); all 128-byte swizzled, so that ldmatrix reads of 8 rows
+// hit 8 distinct bank groups. The y values a lane will update are loaded into
+// registers right after griddep_wait, so they arrive while the shrink
+// computes. Both the shrink partial and the expand run on the warp-level
+// tensor cores (warp_mma.cuh).
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -73,18 +72,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
 
 template <int BN>
 struct FusedGeo {
-  static constexpr int CU = 64 / BN;   // output columns per expand unit (128 bytes of B)
-  static constexpr int CP = CU / 2;    // column pairs per unit
+  static constexpr int CU = 64 / BN;   // output columns per 128-byte B row
   static constexpr int TB = kTileRows * BN;   // partial values per block
 };
 
 struct FusedLayout {
   int nst;           // ring depth
   int cols;          // output columns per block (multiple of 8)
-  int units;         // expand units per block (cols / CU), one 128-byte B row each
-  int box_rows;      // B rows per TMA box (<= 256)
+  int box_rows;      // B rows (128 bytes) per TMA box (<= 256)
   int nbox;          // B boxes per block
-  size_t ring_off, part_off, zd_off, b_off, bytes;   // from the 1024-aligned base
+  size_t ring_off, part_off, zb_off, b_off, bytes;   // from the 1024-aligned base
 };
 
 template <int BN>
@@ -94,24 +91,25 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   const int nkb = (int)((Ks + kShrinkKB - 1) / kShrinkKB);
   L.nst = nkb < kShrinkStages ? nkb : kShrinkStages;
   L.cols = (int)(((N + S - 1) / S + 7) / 8 * 8);
-  L.units = L.cols / F::CU;
-  L.box_rows = L.units < 256 ? L.units : 256;
-  L.nbox = (L.units + L.box_rows - 1) / L.box_rows;
-  L.ring_off = 256;
+  const int brows = L.cols / F::CU;
+  L.box_rows = brows < 256 ? brows : 256;
+  L.nbox = (brows + L.box_rows - 1) / L.box_rows;
+  L.ring_off = 1024;
   L.part_off = L.ring_off + (size_t)L.nst * PartialRing<BN>::kStageBytes;
-  L.zd_off = L.part_off + (size_t)S * F::TB * 4;
-  L.b_off = (L.zd_off + (size_t)F::TB * 8 + 1023) / 1024 * 1024;
+  L.zb_off = L.part_off + (size_t)S * F::TB * 4;
+  L.b_off = (L.zb_off + (size_t)3 * F::TB * 2 + 1023) / 1024 * 1024;
   L.bytes = L.b_off + (size_t)L.nbox * L.box_rows * 128;
   return L;
 }
 
 template <int BN>
 __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
-    fused_fma_kernel(const __grid_constant__ FusedParams p) {
+    fused_warp_kernel(const __grid_constant__ FusedParams p) {
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
-  using F = FusedGeo<BN>;
-  constexpr int CU = F::CU, CP = F::CP, TB = F::TB;
-  using YV = typename std::conditional<CU == 4, uint2, uint4>::type;   // CU bf16 of y
+  constexpr int W = ShrinkGeo<BN>::WARPS;
+  constexpr int TB = FusedGeo<BN>::TB;
+  constexpr int CU = FusedGeo<BN>::CU;
+  constexpr int kPre = 16;   // y words prefetched per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -121,8 +119,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   uint64_t* bar_part = bars + kShrinkStages + 1;                 // incoming partials
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);        // tile entry
   float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [S][8][BN]
-  float2* zd = reinterpret_cast<float2*>(smem + lay.zd_off);     // [8][BN] (z, z)
-  uint8_t* sB = smem + lay.b_off;                                // [units][128 B], swizzled
+  uint16_t* zb = reinterpret_cast<uint16_t*>(smem + lay.zb_off); // [3][8][BN] bf16 parts of Z
+  uint8_t* sB = smem + lay.b_off;                                // 128-byte rows, swizzled
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
@@ -134,7 +132,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
   if (tid == 0) {
     prefetch_tensormap(&p.tm_x);
-    prefetch_tensormap(&p.tm_a);
+    prefetch_tensormap(p.has_a3 ? &p.tm_a3 : &p.tm_a);
     prefetch_tensormap(&p.tm_b);
     for (int i = 0; i < lay.nst; ++i) mbar_init(&bars[i], 1);
     mbar_init(bar_b, 1);
@@ -146,7 +144,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   const int g = ent_s[0];
   const int nrows = ent_s[1];
   const int32_t* rows_s = ent_s + 4;
-  const int64_t M = p.M, N = p.N, K = p.K;
+  const int64_t M = p.M, N = p.N;
   const int r = BN;
   if (nrows <= 0) return;  // the whole cluster shares the tile: all exit
 
@@ -166,19 +164,17 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   // this block's output columns [c0, c0 + ncols) of slice sl
   const int64_t c0 = (int64_t)s * lay.cols;
   const int ncols = (int)max((int64_t)0, min((int64_t)lay.cols, N - c0));
-  const int nunits = ncols / CU;
+  const int nblk = ncols / 8;
   const bool early_w = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
 
   PartialArgs pa;
-  pa.x = p.x + (int64_t)s * p.Ks;
-  pa.A = p.A + ((int64_t)g * p.slices + sl) * r * K + (int64_t)s * p.Ks;
   pa.rows = rows_s;
   pa.status = p.status;
-  pa.K = K;
   pa.Ks = p.Ks;
   pa.nrows = nrows;
   pa.tm_x = &p.tm_x;
   pa.tm_a = &p.tm_a;
+  pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)((int64_t)s * p.Ks);
   pa.a_row = (int)(((int64_t)g * p.slices + sl) * r);
   PartialRing<BN> ring;
@@ -196,7 +192,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
         tma_load_2d(sB + (size_t)bi * lay.box_rows * 128, &p.tm_b, 0,
                     b_row0 + bi * lay.box_rows, bar_b);
   };
-  const int64_t ldy = (int64_t)p.slices * N;
 
   if (warp == 0) {
     if (lane == 0)
@@ -218,16 +213,18 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     if (!early_w) issue_b();
   }
 
-  // y of the thread's first expand unit (all tile rows), loaded now so that
-  // it arrives during the shrink
-  YV ypre[kTileRows];
-  if (tid < nunits) {
+  // Expand geometry: warp w takes the 8-column blocks w, w + W, ...; lane
+  // 4g + t updates row g, columns 2t and 2t+1 of each (one bf16 pair of y).
+  // Its first kPre pairs are loaded now and arrive during the shrink.
+  const int gq = lane >> 2, tq = lane & 3;
+  const bool has_row = gq < nrows;
+  __nv_bfloat16* yrow = p.y + (int64_t)rows_s[min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
+                        (int64_t)sl * N + c0 + 2 * tq;
+  uint32_t ypre[kPre];
 #pragma unroll
-    for (int rr = 0; rr < kTileRows; ++rr)
-      if (rr < nrows)
-        ypre[rr] = *reinterpret_cast<const YV*>(p.y + (int64_t)rows_s[rr] * ldy +
-                                                (int64_t)sl * N + c0 + CU * tid);
-  }
+  for (int i = 0; i < kPre; ++i)
+    if (has_row && warp + i * W < nblk)
+      ypre[i] = *reinterpret_cast<const uint32_t*>(yrow + (warp + i * W) * 8);
 
   float v;
   const bool ok = ring.run(pa, v);
@@ -237,79 +234,82 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   // failed copy), so every block receives exactly S * TB * 4 bytes.
   cluster_wait();
   {
-    const int o = (lane / 4) * BN + warp * ShrinkGeo<BN>::JPW + lane % 4;
     const float pv = ok ? v : 0.0f;
     for (int q = 0; q < S; ++q)
-      st_async_f32(map_rank(part + s * TB + o, (uint32_t)q), pv, map_rank(bar_part, (uint32_t)q));
+      st_async_f32(map_rank(part + s * TB + tid, (uint32_t)q), pv,
+                   map_rank(bar_part, (uint32_t)q));
   }
   // The wait outlasts any sender's own bounded waits, so a block never
   // leaves while a partial is still on its way to it.
   const bool got = mbar_wait_bounded(bar_part, 0, p.status, 1ll << 36);
 
   // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
-  for (int o = tid; o < nrows * BN; o += kThreads) {
-    float total = 0.0f;
-    for (int q = 0; q < S; ++q) total += part[q * TB + o];
-    const float zv = total * p.scale;
-    const float zb = (p.flags & IG_FLAG_Z_FP32) ? zv : bf16_round_f32(zv);
-    zd[o] = make_float2(zb, zb);
-    if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
+  // Thread o owns output o (token row o / r, rank o % r).
+  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
+  {
+    const int o = tid;
+    uint16_t hi = 0, mid = 0, lo = 0;
+    if (o < nrows * BN) {
+      float total = 0.0f;
+      for (int q = 0; q < S; ++q) total += part[q * TB + o];
+      const float zv = total * p.scale;
+      if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
+      split_z(zv, zf32, hi, mid, lo);
+    }
+    zb[o] = hi;
+    zb[TB + o] = mid;
+    zb[2 * TB + o] = lo;
   }
-  __syncthreads();   // zd complete
+  __syncthreads();   // zb complete
 
-  // Expand this block's columns: y = bf16_rn(f32(y) + sum_j zb_j B_nj), the
-  // j sum a chain of FMAs in increasing j (two columns per f32x2 FMA). A unit
-  // is CU consecutive columns for all rows of the tile: its B values are
-  // converted once and used for every row. Every element is computed by one
-  // thread, so the split does not change any result.
+  // Expand this block's columns: y = bf16_rn(f32(y) + D), D the tensor-core
+  // sum over j of bf16(z_j) B_nj (warp_mma.cuh, the same routine as the
+  // two-kernel expand). Every element is computed by one MMA of one warp, so
+  // the split over warps and blocks does not change any result.
   const bool copies_ok = mbar_wait_bounded(bar_b, 0, p.status);
   if (copies_ok && got) {
-    for (int u = tid, k = 0; u < nunits; u += kThreads, ++k) {
-      float2 bp[CP][BN];   // (B[c][j], B[c+1][j]) for column pair c = 2cp
-      {
-        const uint8_t* row = sB + (size_t)u * 128;
-        const int sw = u & 7;   // 128-byte swizzle: 16-byte chunk i sits at i ^ (row % 8)
+    const uint32_t sB_addr = smem_u32(sB);
+    const int parts = zf32 ? 3 : 1;
+    auto store = [&](int blk, uint32_t yv, const float (&d)[4]) {
+      if (has_row)
+        *reinterpret_cast<uint32_t*>(yrow + blk * 8) =
+            f32_to_bf16_bits(bf16lo(yv) + d[0]) | (f32_to_bf16_bits(bf16hi(yv) + d[1]) << 16);
+    };
+    if (!zf32) {
+      // the warp's first kPre blocks, 8 at a time: B operands of all 8, then
+      // their MMAs, then the y updates (the MMA of each block is the one
+      // expand_block_mma issues)
+      ExpandFrag<BN> zf;
+      zf.load_z(zb, lane);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 w = *reinterpret_cast<const uint4*>(row + ((i ^ sw) << 4));
-          float f[8];
-          unpack8(w, f);
-          const int cc = (8 * i) / BN, jb = (8 * i) % BN;
+      for (int h = 0; h < kPre; h += 8) {
+        if (warp + h * W >= nblk) break;
+        uint32_t bq[8][2];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (cc % 2 == 0) bp[cc / 2][jb + e].x = f[e];
-            else bp[cc / 2][jb + e].y = f[e];
-          }
-        }
+        for (int i = 0; i < 8; ++i)
+          ExpandFrag<BN>::load_b(sB_addr, min(warp + (h + i) * W, nblk - 1) * 8, lane, bq[i]);
+        float dq[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) zf.mma(dq[i], bq[i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (warp + (h + i) * W < nblk) store(warp + (h + i) * W, ypre[h + i], dq[i]);
       }
+    } else {
 #pragma unroll
-      for (int rr = 0; rr < kTileRows; ++rr) {
-        if (rr >= nrows) break;
-        __nv_bfloat16* yp = p.y + (int64_t)rows_s[rr] * ldy + (int64_t)sl * N + c0 + CU * u;
-        const YV yv = k == 0 ? ypre[rr] : *reinterpret_cast<const YV*>(yp);
-        float2 acc[CP];
-#pragma unroll
-        for (int cp = 0; cp < CP; ++cp) acc[cp] = make_float2(0.0f, 0.0f);
-        const float4* zr = reinterpret_cast<const float4*>(zd + rr * BN);
-#pragma unroll
-        for (int jj = 0; jj < BN / 2; ++jj) {
-          const float4 z2 = zr[jj];   // (z_j, z_j, z_j+1, z_j+1)
-#pragma unroll
-          for (int cp = 0; cp < CP; ++cp)
-            acc[cp] = __ffma2_rn(make_float2(z2.x, z2.y), bp[cp][2 * jj], acc[cp]);
-#pragma unroll
-          for (int cp = 0; cp < CP; ++cp)
-            acc[cp] = __ffma2_rn(make_float2(z2.z, z2.w), bp[cp][2 * jj + 1], acc[cp]);
-        }
-        const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
-        YV out;
-        uint32_t* ow = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-        for (int cp = 0; cp < CP; ++cp)
-          ow[cp] = f32_to_bf16_bits(bf16lo(yw[cp]) + acc[cp].x) |
-                   (f32_to_bf16_bits(bf16hi(yw[cp]) + acc[cp].y) << 16);
-        *reinterpret_cast<YV*>(yp) = out;
+      for (int i = 0; i < kPre; ++i) {
+        const int blk = warp + i * W;
+        if (blk >= nblk) break;
+        float d[4];
+        expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
+        store(blk, ypre[i], d);
       }
+    }
+    // blocks past the prefetched ones (more than kPre per warp)
+    for (int blk = warp + kPre * W; blk < nblk; blk += W) {
+      float d[4];
+      expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
+      store(blk, has_row ? *reinterpret_cast<const uint32_t*>(yrow + blk * 8) : 0u, d);
     }
   }
   // a copy that never completed: wait for it once more (bounded) before the
@@ -328,12 +328,12 @@ int fused_b_box_rows(int bn, int64_t Ks, int64_t N, int S) {
   return bn == 16 ? fused_layout<16>(Ks, N, S).box_rows : fused_layout<8>(Ks, N, S).box_rows;
 }
 
-cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st) {
+cudaError_t launch_fused_warp(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st) {
   const int64_t grid = tiles_max * p.slices * p.S;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = fused_smem_bytes(bn, p.Ks, p.N, p.S);
-  void (*kern)(FusedParams) = bn == 16 ? fused_fma_kernel<16> : fused_fma_kernel<8>;
+  void (*kern)(FusedParams) = bn == 16 ? fused_warp_kernel<16> : fused_warp_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

@@ -42,18 +42,16 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) {
   return (v + a - 1) / a * a;
 }
 
-// FMA-path geometry (fixed: part of the determinism key where it sets the
-// arithmetic order).
-constexpr int kTileRows = 8;           // token rows per tile of the tile table
+// Small-rank (warp-MMA) path geometry (fixed: part of the determinism key
+// where it sets the arithmetic order).
+constexpr int kTileRows = 8;           // token rows per tile of the tile table (the MMA's N)
 constexpr int kTileInts = 4 + kTileRows;  // [g, nrows, consecutive, 0, rows[8]] = 48 bytes
-constexpr int kShrinkKB = 256;        // elements per k-block: 32 lanes x 8
+constexpr int kShrinkKB = 256;        // elements per k-block (4 swizzled sub-blocks of 64)
 constexpr int kShrinkStages = 4;
 constexpr int kExpandWarps = 4;
-constexpr int kExpandRowsPerWarp = 2;
-constexpr int kExpandBM = kExpandWarps * kExpandRowsPerWarp;  // 16 = kTileRows
-constexpr int kExpandBN = 256;        // output columns: 32 lanes x 8
-constexpr int kExpandJC = 16;         // rank elements per register chunk
-static_assert(kExpandBM == kTileRows, "tile rows");
+constexpr int kExpandBN = 256;        // output columns per expand block: 4 warps x 8 blocks of 8
+// Revision of the arithmetic of the kernels; part of the determinism key.
+constexpr int kArithRevision = 2;
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
@@ -80,8 +78,9 @@ struct MapParams {
 };
 
 struct ShrinkParams {
-  CUtensorMap tm_x;     // x [M][K], box 256 x 1 (row gathers)
-  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 256 x BN
+  CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x BN, 128-byte swizzle
+  CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, BN, 4} (when has_a3)
   const __nv_bfloat16* x;
   const __nv_bfloat16* A;
   const int32_t* tiles;
@@ -91,10 +90,12 @@ struct ShrinkParams {
   uint32_t* status;
   int64_t M, K, r, Ks;
   int32_t slices, L, S, jblocks, flags;
+  int32_t has_a3;       // K and K/S multiples of 64: one 3-D copy per k-block of A
   float scale;
 };
 
 struct ExpandParams {
+  CUtensorMap tm_b;     // B_stack as rows of 64 elements, box 64 x box_rows, 128-byte swizzle
   const float* z;
   const __nv_bfloat16* B;
   const int32_t* tiles;
@@ -109,10 +110,17 @@ struct ExpandParams {
 // IG_ERR_CUDA (driver entry point missing or encode rejected).
 int encode_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                   uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows, int swizzle);
+// A_stack [rows][K] (K % 64 == 0) seen as a 3-D bf16 tensor {64, rows, K / 64}
+// with strides {K * 2, 128} bytes: a box {64, box_rows, 4} brings 4
+// consecutive 64-element sub-blocks of box_rows rows, stored sub-block by
+// sub-block, 128-byte swizzled. IG_OK or IG_ERR_CUDA.
+int encode_map_a3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
+                  uint32_t box_rows);
 
 struct FusedParams {
-  CUtensorMap tm_x;     // x [M][K], box 256 x 1 (row gathers)
-  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 256 x r
+  CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
+  CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, r, 4} (when has_a3)
   CUtensorMap tm_b;     // B_stack as rows of 64 elements (64/r output columns
                         // x r), box 64 x b_box_rows, 128-byte swizzle
   const __nv_bfloat16* x;
@@ -125,6 +133,7 @@ struct FusedParams {
   int64_t M, K, N, Ks;
   int32_t slices, L, S, flags;
   int32_t b_box_rows;
+  int32_t has_a3;
   float scale;
 };
 
@@ -165,13 +174,15 @@ struct TreeParams {
 
 // Launchers (defined in the .cu files); they return cudaGetLastError().
 cudaError_t launch_map_tokens(const MapParams& p, cudaStream_t st);
-cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn,
+cudaError_t launch_shrink_warp(const ShrinkParams& p, int mode, int bn,
                               int64_t tiles_max, cudaStream_t st);
-cudaError_t launch_expand_fma(const ExpandParams& p, int64_t tiles_max,
+cudaError_t launch_expand_warp(const ExpandParams& p, int64_t tiles_max,
                               cudaStream_t st);
-cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st);
+cudaError_t launch_fused_warp(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st);
 size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S);
 int fused_b_box_rows(int bn, int64_t Ks, int64_t N, int S);
+size_t expand_warp_smem_bytes(int r, int64_t N);
+int expand_warp_box_rows(int r, int64_t N);
 cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
                               cudaStream_t st);
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st);
@@ -281,6 +292,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+        "r"(smem_u32(bar)) : "memory");
+}
+// Tiled 3-D tensor copy global -> shared (box at coordinates {c0, c1, c2},
+// innermost first); c0 * 2 bytes must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
         "r"(smem_u32(bar)) : "memory");
 }
 // Row gather: four rows r0..r3 of a 2-D tensor map whose box is one row high,

@@ -1,51 +1,48 @@
-// The shrink partial of one tile over one K partition, on CUDA cores. Shared
-// by the Split-K shrink kernel and the fused decode kernel so that both
-// compute bit-identical partials.
+// The shrink partial of one tile over one K partition, on the warp-level
+// tensor cores. Shared by the Split-K shrink kernel and the fused decode
+// kernel so that both compute bit-identical partials.
 //
-// Tile: up to 8 token rows x BN rank columns (BN = 8 or 16). The block has
-// BN/4 warps; warp w computes rank columns 4w .. 4w+3 for all 8 rows (32
-// outputs), so every lane ends with exactly one finished output and every
-// warp has work however few rows the tile holds. The partition [k0, k0 + Ks) is streamed through a ring of
-// `nst` shared-memory stages, k-blocks of 256 elements, completion counted in
-// bytes on one mbarrier per stage; warp 0 issues the copies. Two ways to
-// copy: with tensor maps, one tiled TMA copy brings the A block (BN rows)
-// and one row-gather TMA copy per 4 token rows brings x (boxes are always
-// 256 wide; columns past the partition are loaded but not used); without,
-// one 1-D bulk copy per row.
+// Tile: up to 8 token rows x BN rank columns (BN = 8 or 16); the block has
+// BN/4 warps (4 or 2) and ends with one output per thread: thread o holds
+// the partial of token row o / BN, rank o % BN. The partition [k0, k0 + Ks)
+// is streamed through a ring of `nst` shared-memory stages of 256 elements,
+// each stage four 64-element sub-blocks written by TMA copies with 128-byte
+// swizzle (the BN A rows of all four sub-blocks by one 3-D tiled copy when
+// K and K/S are multiples of 64, else one 2-D copy per sub-block; one row
+// gather per 4 token rows per sub-block; completion counted in bytes on one
+// mbarrier per stage); warp 0 issues the copies.
 //
 // Order of the sum, identical for every row and every M ("Reproducible LoRA
 // Inference Through Deterministic Split-K Reduction" leaves the order inside
-// a partition to the kernel, sec. 4.3): lane l owns the 8-element chunks
-// l, l+32, ... of the partition and accumulates them in increasing k with FMA
-// (two independent FMAs per packed f32x2 instruction, each rounded like
-// fmaf); the 32 lane sums are then combined by a fixed xor butterfly
-// (16, 8, 4, 2, 1) as a reduce-scatter. Neither the number of rows a warp
-// holds nor which warp holds a row changes a row's arithmetic.
+// a partition to the kernel, sec. 4.3): the partition is cut into 16-element
+// steps (an 8-element step last when Ks % 16 == 8); step i of a 256-element
+// block belongs to warp i % W. Each warp accumulates its steps in increasing
+// k with bf16 tensor-core MMAs into FP32 (m16n8k16: 16 ranks x 8 tokens x 16
+// k per instruction; ranks 8..15 are zero when BN = 8). The W warp sums are
+// then added in warp order: ((D0 + D1) + D2) + D3. A token's value depends
+// only on its own x row: the MMA's columns are independent.
 #pragma once
 
-#include "ig_common.cuh"
+#include "warp_mma.cuh"
 
 namespace ig {
 
 template <int BN>
 struct ShrinkGeo {
-  static constexpr int JPW = 4;                   // rank columns per warp
-  static constexpr int WARPS = BN / JPW;          // 4 for BN = 16, 2 for BN = 8
+  static constexpr int WARPS = BN / 4;            // 4 for BN = 16, 2 for BN = 8
   static constexpr int THREADS = WARPS * 32;
-  static_assert(kTileRows * JPW == 32 && WARPS * JPW == BN, "shrink geometry");
+  static constexpr int TB = kTileRows * BN;       // outputs per tile = threads
+  static_assert(TB == THREADS, "one output per thread");
 };
 
 struct PartialArgs {
-  const __nv_bfloat16* x;     // x + k0
-  const __nv_bfloat16* A;     // first A row of the tile's column block, + k0
   const int32_t* rows;        // token rows of the tile (shared memory)
   uint32_t* status;
-  int64_t K;                  // row stride of x and A, in elements
   int64_t Ks;                 // partition length
   int nrows;
-  // tensor-map copies (both null: 1-D bulk copies)
-  const CUtensorMap* tm_x;    // x [M][K], box 256 x 1
-  const CUtensorMap* tm_a;    // A as [rows][K], box 256 x BN
+  const CUtensorMap* tm_x;    // x [M][K], box 64 x 1, 128-byte swizzle
+  const CUtensorMap* tm_a;    // A as [rows][K], box 64 x BN, 128-byte swizzle
+  const CUtensorMap* tm_a3;   // A as {64, rows, K/64}, box {64, BN, 4}, or null
   int k0;                     // partition start (column coordinate)
   int a_row;                  // row coordinate of the tile's first A row
 };
@@ -53,67 +50,67 @@ struct PartialArgs {
 template <int BN>
 struct PartialRing {
   using G = ShrinkGeo<BN>;
-  static constexpr int kRowBytes = kShrinkKB * 2;                  // 512
-  static constexpr int kStageBytes = (kTileRows + BN) * kRowBytes;
-  uint8_t* stages;
+  static constexpr int kSub = kShrinkKB / 64;                 // 64-element sub-blocks
+  static constexpr int kXBytes = kSub * kTileRows * 128;      // [sub][8 rows][128 B]
+  static constexpr int kABytes = kSub * BN * 128;             // [sub][BN rows][128 B]
+  static constexpr int kStageBytes = kXBytes + kABytes;       // multiple of 1024
+  uint8_t* stages;   // 1024-aligned
   uint64_t* bars;
   int nst;      // ring depth
   int nkb;      // k-blocks in the partition
 
-  __device__ __forceinline__ uint32_t block_bytes(const PartialArgs& a, int b) const {
-    return (uint32_t)(min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB) * 2);
+  __device__ __forceinline__ int klen(const PartialArgs& a, int b) const {
+    return (int)min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB);
+  }
+  __device__ __forceinline__ int nsub(const PartialArgs& a, int b) const {
+    return (klen(a, b) + 63) / 64;
   }
   // warp 0: arm stage b % nst for all copies of k-block b
   __device__ __forceinline__ void expect(const PartialArgs& a, int b) const {
-    uint32_t bytes;
-    if (a.tm_x) bytes = (uint32_t)kRowBytes * (BN + 4 * ((a.nrows + 3) / 4));
-    else bytes = block_bytes(a, b) * (uint32_t)(a.nrows + BN);
+    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * (BN + 4 * ((a.nrows + 3) / 4));
     if ((threadIdx.x & 31) == 0) mbar_arrive_expect_tx(&bars[b % nst], bytes);
     __syncwarp();
   }
   __device__ __forceinline__ void issue_a(const PartialArgs& a, int b) const {
-    const int lane = threadIdx.x & 31;
+    if ((threadIdx.x & 31) != 0) return;
     const int st = b % nst;
-    uint8_t* sa = stages + st * kStageBytes + kTileRows * kRowBytes;
-    if (a.tm_a) {
-      if (lane == 0) tma_load_2d(sa, a.tm_a, a.k0 + b * kShrinkKB, a.a_row, &bars[st]);
+    uint8_t* sa = stages + st * kStageBytes + kXBytes;
+    const int ns = nsub(a, b);
+    if (a.tm_a3 && ns == kSub) {   // the four sub-blocks in one copy (same layout)
+      tma_load_3d(sa, a.tm_a3, 0, a.a_row, (a.k0 + b * kShrinkKB) / 64, &bars[st]);
       return;
     }
-    const uint32_t bytes = block_bytes(a, b);
-    for (int j = lane; j < BN; j += 32)
-      bulk_g2s(sa + j * kRowBytes, a.A + (int64_t)j * a.K + (int64_t)b * kShrinkKB, bytes,
-               &bars[st]);
+    for (int q = 0; q < ns; ++q)
+      tma_load_2d(sa + q * BN * 128, a.tm_a, a.k0 + b * kShrinkKB + q * 64, a.a_row, &bars[st]);
   }
   __device__ __forceinline__ void issue_x(const PartialArgs& a, int b) const {
     const int lane = threadIdx.x & 31;
     const int st = b % nst;
     uint8_t* sx = stages + st * kStageBytes;
-    if (a.tm_x) {
-      // rows past nrows repeat the last row: loaded, never used
-      if (4 * lane < a.nrows) {
-        const int last = a.nrows - 1;
-        tma_gather4(sx + 4 * lane * kRowBytes, a.tm_x, a.k0 + b * kShrinkKB,
-                    a.rows[min(4 * lane, last)], a.rows[min(4 * lane + 1, last)],
-                    a.rows[min(4 * lane + 2, last)], a.rows[min(4 * lane + 3, last)], &bars[st]);
-      }
-      return;
+    const int groups4 = (a.nrows + 3) / 4;
+    const int last = a.nrows - 1;
+    // one lane per (sub-block, group of 4 rows); rows past nrows repeat the
+    // last row: loaded, never used
+    if (lane < nsub(a, b) * groups4) {
+      const int q = lane / groups4, gq = lane % groups4;
+      tma_gather4(sx + q * 1024 + gq * 512, a.tm_x, a.k0 + b * kShrinkKB + q * 64,
+                  a.rows[min(4 * gq, last)], a.rows[min(4 * gq + 1, last)],
+                  a.rows[min(4 * gq + 2, last)], a.rows[min(4 * gq + 3, last)], &bars[st]);
     }
-    const uint32_t bytes = block_bytes(a, b);
-    for (int i = lane; i < a.nrows; i += 32)
-      bulk_g2s(sx + i * kRowBytes, a.x + (int64_t)a.rows[i] * a.K + (int64_t)b * kShrinkKB,
-               bytes, &bars[st]);
   }
 
   // All threads. The first min(nkb, nst) k-blocks must already be armed and
-  // issued. On return `out` is this lane's output: row lane/4, column
-  // 4*warp + lane%4 (not yet scaled). Returns false if a copy wait expired
+  // issued. On return `out` is this thread's output: token row tid / BN,
+  // rank tid % BN (not yet scaled). Returns false if a copy wait expired
   // (after draining, bounded, every copy still in flight).
   __device__ __forceinline__ bool run(const PartialArgs& a, float& out) const {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j0 = warp * G::JPW;
-    float2 acc[kTileRows][2];   // [row][column pair]
-#pragma unroll
-    for (int rr = 0; rr < kTileRows; ++rr) acc[rr][0] = acc[rr][1] = make_float2(0.0f, 0.0f);
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // ldmatrix row addresses of this lane: A (ranks) rows and x (tokens) rows
+    const int arow = (lane & 7) + (BN == 16 ? 8 * ((lane >> 3) & 1) : 0);
+    const int achunk = BN == 16 ? (lane >> 4) : ((lane >> 3) & 1);
+    const int xrow = lane & 7;
+    const int xchunk = (lane >> 3) & 1;
 
     int issued = min(nkb, nst);
     int fail_b = -1;
@@ -122,34 +119,52 @@ struct PartialRing {
       const uint32_t parity = (uint32_t)((b / nst) & 1);
       const bool ok = mbar_wait_bounded(&bars[st], parity, a.status);
       if (__syncthreads_or(!ok)) { fail_b = b; break; }
-      const int64_t klen = min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB);
-      if ((int64_t)lane * 8 < klen) {
-        const uint8_t* sx = stages + st * kStageBytes;
-        const uint8_t* sa = sx + kTileRows * kRowBytes;
-        float2 aa[2][8];   // columns (j0, j0+1) and (j0+2, j0+3), element e
-#pragma unroll
-        for (int jp = 0; jp < 2; ++jp) {
-          const uint4 u0 = *reinterpret_cast<const uint4*>(sa + (j0 + 2 * jp) * kRowBytes + lane * 16);
-          const uint4 u1 = *reinterpret_cast<const uint4*>(sa + (j0 + 2 * jp + 1) * kRowBytes + lane * 16);
-          float a0[8], a1[8];
-          unpack8(u0, a0);
-          unpack8(u1, a1);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) aa[jp][e] = make_float2(a0[e], a1[e]);
+      const int kl = klen(a, b);
+      const int n16 = kl / 16;
+      const uint32_t sx = smem_u32(stages + st * kStageBytes);
+      const uint32_t sa = sx + kXBytes;
+      // operands of step kk (16 elements): A fragment (ranks) and x fragment (tokens)
+      auto frag = [&](int kk, uint32_t (&af)[4], uint32_t (&bf)[2]) {
+        const int q = kk >> 2, c16 = (kk & 3) * 2;    // sub-block, first 16-byte chunk
+        if (BN == 16) {
+          ldsm_x4(sa + q * BN * 128 + arow * 128 + (((c16 + achunk) ^ (arow & 7)) << 4),
+                  af[0], af[1], af[2], af[3]);
+        } else {
+          ldsm_x2(sa + q * BN * 128 + arow * 128 + (((c16 + achunk) ^ (arow & 7)) << 4),
+                  af[0], af[2]);
+          af[1] = af[3] = 0u;
         }
+        ldsm_x2(sx + q * 1024 + xrow * 128 + (((c16 + xchunk) ^ xrow) << 4), bf[0], bf[1]);
+      };
+      if (kl == kShrinkKB) {
+        // full k-block: this warp's 16 / W steps, all operands first, then the
+        // MMAs in step order (the same sequence as the loop below)
+        constexpr int NS = 16 / G::WARPS;
+        uint32_t af[NS][4], bf[NS][2];
 #pragma unroll
-        for (int rr = 0; rr < kTileRows; ++rr) {
-          if (rr >= a.nrows) break;
-          const uint4 u = *reinterpret_cast<const uint4*>(sx + rr * kRowBytes + lane * 16);
-          float xv[8];
-          unpack8(u, xv);
+        for (int i = 0; i < NS; ++i) frag(warp + i * G::WARPS, af[i], bf[i]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 xx = make_float2(xv[e], xv[e]);
-            acc[rr][0] = __ffma2_rn(xx, aa[0][e], acc[rr][0]);
-            acc[rr][1] = __ffma2_rn(xx, aa[1][e], acc[rr][1]);
-          }
+        for (int i = 0; i < NS; ++i)
+          mma_16816(d, af[i][0], af[i][1], af[i][2], af[i][3], bf[i][0], bf[i][1]);
+      } else {
+        for (int kk = warp; kk < n16; kk += G::WARPS) {
+          uint32_t af[4], bf[2];
+          frag(kk, af, bf);
+          mma_16816(d, af[0], af[1], af[2], af[3], bf[0], bf[1]);
         }
+      }
+      if ((kl & 15) && warp == n16 % G::WARPS) {
+        // the last 8 elements of the partition
+        const int q = n16 >> 2, c = (n16 & 3) * 2;
+        uint32_t a0, a1, b0;
+        if (BN == 16) {
+          ldsm_x2(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0, a1);
+        } else {
+          ldsm_x1(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0);
+          a1 = 0u;
+        }
+        ldsm_x1(sx + q * 1024 + xrow * 128 + ((c ^ xrow) << 4), b0);
+        mma_1688(d, a0, a1, b0);
       }
       __syncthreads();
       if (b + nst < nkb) {
@@ -169,29 +184,21 @@ struct PartialRing {
       return false;
     }
 
-    // Reduce-scatter: 32 values per lane (row-major rr*4 + j) -> one per lane.
-    float v[32];
-#pragma unroll
-    for (int rr = 0; rr < kTileRows; ++rr) {
-      v[rr * 4 + 0] = acc[rr][0].x;
-      v[rr * 4 + 1] = acc[rr][0].y;
-      v[rr * 4 + 2] = acc[rr][1].x;
-      v[rr * 4 + 3] = acc[rr][1].y;
+    // Warp sums -> shared memory (stage 0, no copy in flight any more), then
+    // thread o adds the W values of output o in warp order.
+    float* red = reinterpret_cast<float*>(stages);
+    const int g = lane >> 2, t = lane & 3;
+    red[warp * G::TB + (2 * t) * BN + g] = d[0];
+    red[warp * G::TB + (2 * t + 1) * BN + g] = d[1];
+    if (BN == 16) {
+      red[warp * G::TB + (2 * t) * BN + g + 8] = d[2];
+      red[warp * G::TB + (2 * t + 1) * BN + g + 8] = d[3];
     }
+    __syncthreads();
+    float v = red[tid];
 #pragma unroll
-    for (int lvl = 0; lvl < 5; ++lvl) {
-      const int off = 16 >> lvl;
-      const int half = 32 >> (lvl + 1);
-      const bool upper = (lane & off) != 0;
-#pragma unroll
-      for (int i = 0; i < half; ++i) {
-        const float send = upper ? v[i] : v[i + half];
-        const float keep = upper ? v[i + half] : v[i];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-        v[i] = keep + recv;
-      }
-    }
-    out = v[0];
+    for (int w = 1; w < G::WARPS; ++w) v += red[w * G::TB + tid];
+    out = v;
     return true;
   }
 };

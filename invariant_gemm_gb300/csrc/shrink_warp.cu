@@ -1,4 +1,5 @@
-// LoRA shrink on CUDA cores: Z = scale * X A_i^T with a Split-K reduction.
+// LoRA shrink for small ranks: Z = scale * X A_i^T with a Split-K reduction,
+// the partials on the warp-level tensor cores (shrink_core.cuh).
 //
 // "Reproducible LoRA Inference Through Deterministic Split-K Reduction":
 //   Eq. 3 / Fig. 1  S thread blocks per output tile, block s sums over the
@@ -12,24 +13,21 @@
 //   sec. 4.2        UNSPLIT: S = 1, one block over the whole of K;
 //   sec. 4.3        DET_TREE: partials only, combined by reduce_tree.cu.
 //
-// Block = BN/4 warps (warp w: rank columns 4w .. 4w+3 of all rows), tile =
-// up to 8 token rows of one adapter (one entry of the token
-// map's tile table) x BN rank columns, one K partition. The partition
-// is streamed through shared memory in k-blocks of 256 elements by TMA
-// copies (one tiled copy for the A block, one row gather per 4 token rows,
-// completion counted on an mbarrier), four stages deep.
+// Block = BN/4 warps, tile = up to 8 token rows of one adapter (one entry of
+// the token map's tile table) x BN rank columns, one K partition; thread o
+// ends with the output of token row o / BN, rank o % BN. The partition is
+// streamed through shared memory in k-blocks of 256 elements by TMA copies
+// (completion counted on an mbarrier), four stages deep.
 //
 // Latency: the tile entry is read before griddep_wait() (the token map is
 // complete before this kernel starts); with IG_FLAG_STATIC_WEIGHTS the A
 // rows of the first stages are requested before it too, so only the x rows
 // wait for the previous kernel.
 //
-// Reduction order inside a partition, identical for every row and every M:
-//   lane l owns the 8-element chunks l, l+32, l+64, ... of the partition and
-//   accumulates their elements in increasing k with FMA into one FP32
-//   register per output; the 32 lane sums are then combined by a fixed
-//   butterfly (xor 16, 8, 4, 2, 1), done as a reduce-scatter so each lane
-//   ends with NV/32 finished outputs. It depends only on K/S.
+// Reduction order inside a partition (shrink_core.cuh): 16-element steps
+// dealt round-robin to the warps, each warp's steps accumulated in increasing
+// k by bf16 MMAs into FP32, then the warp sums added in warp order. It
+// depends only on K/S and BN.
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -38,22 +36,25 @@ namespace {
 
 template <int BN>
 struct ShrinkSmem {
-  static constexpr int kStagesOff = 256;                           // mbarriers + info
-  static constexpr int kBytes = kStagesOff + kShrinkStages * PartialRing<BN>::kStageBytes;
+  static constexpr int kStagesOff = 1024;                          // mbarriers + info
+  // + 1024: the base is aligned to 1024 bytes (128-byte swizzle atoms)
+  static constexpr int kBytes = 1024 + kStagesOff + kShrinkStages * PartialRing<BN>::kStageBytes;
 };
 
 template <int BN, int MODE>
 __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
-    shrink_fma_kernel(const __grid_constant__ ShrinkParams p) {
+    shrink_warp_kernel(const __grid_constant__ ShrinkParams p) {
   using SM = ShrinkSmem<BN>;
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);    // tile entry (kTileInts)
   int32_t* info = reinterpret_cast<int32_t*>(smem + 192);
   uint8_t* stages = smem + SM::kStagesOff;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int S = p.S;
 
   int64_t bid = blockIdx.x;
@@ -91,19 +92,16 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     return;
   }
 
-  const int64_t K = p.K;
   const int64_t k0 = (int64_t)s * p.Ks;
   const bool early_a = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
   PartialArgs pa;
-  pa.x = p.x + k0;
-  pa.A = p.A + (((int64_t)g * p.slices + sl) * r + (int64_t)jb * BN) * K + k0;
   pa.rows = rows_s;
   pa.status = p.status;
-  pa.K = K;
   pa.Ks = p.Ks;
   pa.nrows = nrows;
   pa.tm_x = &p.tm_x;
   pa.tm_a = &p.tm_a;
+  pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)k0;
   pa.a_row = (int)(((int64_t)g * p.slices + sl) * r + (int64_t)jb * BN);
   PartialRing<BN> ring;
@@ -130,8 +128,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
 
   float v;
   if (!ring.run(pa, v)) return;
-  const int rrow = lane / 4;                 // this lane's output
-  const int j0 = warp * ShrinkGeo<BN>::JPW + lane % 4;
+  const int rrow = tid / BN;                 // this thread's output
+  const int j0 = tid % BN;
 
   if (MODE == IG_MODE_UNSPLIT || MODE == IG_MODE_ATOMIC) {
     if (rrow < nrows) {
@@ -172,7 +170,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
 template <int BN, int MODE>
 cudaError_t launch_one(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
   using SM = ShrinkSmem<BN>;
-  auto kern = shrink_fma_kernel<BN, MODE>;
+  auto kern = shrink_warp_kernel<BN, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SM::kBytes);
   if (e != cudaSuccess) return e;
@@ -184,7 +182,7 @@ cudaError_t launch_one(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st
 
 }  // namespace
 
-cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn, int64_t tiles_max,
+cudaError_t launch_shrink_warp(const ShrinkParams& p, int mode, int bn, int64_t tiles_max,
                               cudaStream_t st) {
   if (bn == 16) {
     if (mode == IG_MODE_DET_TREE) return launch_one<16, IG_MODE_DET_TREE>(p, tiles_max, st);

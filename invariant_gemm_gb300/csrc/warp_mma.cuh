@@ -1,0 +1,157 @@
+// Warp-level tensor-core helpers for the small-rank (decode) path: ldmatrix
+// loads and the bf16 mma.sync shapes m16n8k16 / m16n8k8 with FP32
+// accumulation, plus the 128-byte-swizzled shared-memory addressing that the
+// TMA copies of the path produce.
+//
+// Why warp-level MMA here and tcgen05 on the prefill path: a decode tile is
+// 8 tokens x 8 or 16 ranks. tcgen05.mma needs M >= 64 with both operands in
+// shared memory, so most of what it would read would be padding; m16n8k16 is
+// exactly 16 ranks x 8 tokens x 16 k (or 8 tokens x 8 columns x 16 ranks in
+// the expand), with its operands in registers.
+//
+// Fragment layouts (PTX ISA, mma.m16n8k16 / m16n8k8 with .bf16, .row.col),
+// lane = 4 g + t:
+//   A (16 x 16): reg0 (row g, k 2t..2t+1), reg1 (row g+8, k 2t..),
+//                reg2 (row g, k 2t+8..),  reg3 (row g+8, k 2t+8..)
+//   A (16 x 8):  reg0 (row g, k 2t..),    reg1 (row g+8, k 2t..)
+//   B (16 x 8):  reg0 (k 2t..2t+1, col g), reg1 (k 2t+8.., col g)
+//   B (8 x 8):   reg0 (k 2t..2t+1, col g)
+//   D (16 x 8):  d0 (row g, col 2t), d1 (row g, col 2t+1),
+//                d2 (row g+8, col 2t), d3 (row g+8, col 2t+1)
+// ldmatrix .m8n8 gives lane 4g + t the elements 2t, 2t+1 of row g of each
+// 8 x 8 matrix; lanes 8i .. 8i+7 supply the row addresses of matrix i.
+#pragma once
+
+#include "ig_common.cuh"
+
+namespace ig {
+
+// Byte offset of element e (a multiple of 8) in a buffer of 128-byte rows of
+// 64 bf16 written by a TMA copy with 128-byte swizzle (buffer 1024-aligned):
+// the 16-byte chunk q of row R sits at chunk position q ^ (R % 8).
+__device__ __forceinline__ uint32_t swz128(uint32_t e) {
+  const uint32_t R = e >> 6, q = (e >> 3) & 7;
+  return (R << 7) | ((q ^ (R & 7)) << 4);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t& r0) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x1.shared.b16 {%0}, [%1];" : "=r"(r0) : "r"(addr));
+}
+
+// d = A B + d, A 16 x 16, B 16 x 8 (bf16), d FP32 (registers only: not
+// volatile, so the compiler may schedule it; the ldmatrix loads stay volatile
+// to keep them behind the waits that publish their shared memory)
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// d = A B + d, A 16 x 8, B 8 x 8 (bf16), d FP32
+__device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5}, {%6}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Round-to-nearest-even bf16 bits of an FP32 value, as the low half.
+__device__ __forceinline__ uint32_t bf16_bits(float f) { return f32_to_bf16_bits(f); }
+
+// Z split for the expand's A operand: hi = bf16(z); with full FP32 Z also
+// mid = bf16(z - hi) and lo = bf16(z - hi - mid), each difference exact, so
+// that hi + mid + lo == z exactly (24 significant bits = 3 x 8).
+__device__ __forceinline__ void split_z(float z, bool fp32, uint16_t& hi, uint16_t& mid,
+                                        uint16_t& lo) {
+  const uint32_t h = bf16_bits(z);
+  hi = (uint16_t)h;
+  if (!fp32) {
+    mid = lo = 0;
+    return;
+  }
+  const float r1 = z - __uint_as_float(h << 16);
+  const uint32_t m = bf16_bits(r1);
+  const float r2 = r1 - __uint_as_float(m << 16);
+  mid = (uint16_t)m;
+  lo = (uint16_t)bf16_bits(r2);
+}
+
+// One 8-column block of the expand on the tensor cores:
+//   D[m][n] = sum over j of Zb[m][j] * B[cb + n][j],  m < 8 (rows 8..15 zero)
+// j in increasing 16-element chunks (an 8-element chunk last when r % 16 ==
+// 8); with three Z parts (FP32 Z) the hi, mid and lo MMAs of a chunk follow
+// each other. zb: bf16 [parts][8][r] in shared memory; sB: the B columns,
+// column c at elements c * r .. c * r + r - 1 of a 128-byte-swizzled buffer
+// (see swz128). Returns d0 = D[g][2t], d1 = D[g][2t+1].
+__device__ __forceinline__ void expand_block_mma(float (&d)[4], uint32_t sB_addr, int cb,
+                                                 int r, const uint16_t* zb, int parts,
+                                                 int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  d[0] = d[1] = d[2] = d[3] = 0.0f;
+  const int c = cb + (lane & 7);              // the column whose row address this lane gives
+  const int jsel = ((lane >> 3) & 1) * 8;     // matrix 1: elements 8..15 of the chunk
+  const uint32_t* z32 = reinterpret_cast<const uint32_t*>(zb);
+  const int zrow = g * (r / 2);               // this lane's Z row, in bf16 pairs
+  int j = 0;
+  for (; j + 16 <= r; j += 16) {
+    uint32_t b0, b1;
+    ldsm_x2(sB_addr + swz128((uint32_t)(c * r + j + jsel)), b0, b1);
+#pragma unroll 1
+    for (int q = 0; q < parts; ++q) {
+      const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
+      mma_16816(d, zp[0], 0u, zp[4], 0u, b0, b1);
+    }
+  }
+  if (j < r) {   // last 8 elements
+    uint32_t b0;
+    ldsm_x1(sB_addr + swz128((uint32_t)(c * r + j)), b0);
+#pragma unroll 1
+    for (int q = 0; q < parts; ++q) {
+      const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
+      mma_1688(d, zp[0], 0u, b0);
+    }
+  }
+}
+
+// The same MMA as expand_block_mma for r = R (16 or 8) and one Z part, split
+// into its operand loads so that a warp can issue the loads of many blocks
+// before their MMAs.
+template <int R>
+struct ExpandFrag {
+  uint32_t za0, za2;   // Zb fragment: row g, j 2t..2t+1 and j 2t+8..2t+9 (R = 16)
+  __device__ __forceinline__ void load_z(const uint16_t* zb, int lane) {
+    const uint32_t* z32 = reinterpret_cast<const uint32_t*>(zb) + (lane >> 2) * (R / 2) +
+                          (lane & 3);
+    za0 = z32[0];
+    za2 = R == 16 ? z32[4] : 0u;
+  }
+  __device__ __forceinline__ static void load_b(uint32_t sB_addr, int cb, int lane,
+                                                uint32_t (&b)[2]) {
+    const int c = cb + (lane & 7);
+    if (R == 16) {
+      ldsm_x2(sB_addr + swz128((uint32_t)(c * R + ((lane >> 3) & 1) * 8)), b[0], b[1]);
+    } else {
+      ldsm_x1(sB_addr + swz128((uint32_t)(c * R)), b[0]);
+      b[1] = 0u;
+    }
+  }
+  __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&b)[2]) const {
+    d[0] = d[1] = d[2] = d[3] = 0.0f;
+    if (R == 16) mma_16816(d, za0, 0u, za2, 0u, b[0], b[1]);
+    else mma_1688(d, za0, 0u, b[0]);
+  }
+};
+
+}  // namespace ig

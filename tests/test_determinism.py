@@ -295,6 +295,8 @@ FUSED_CASES = [
     (33, 2048, 1024, 16, 1, 4, 2, 0.0),
     (64, 8192, 1024, 16, 2, 4, 16, 0.1),   # 16-block clusters
     (300, 11008, 4096, 8, 1, 6, 8, 0.0),   # K/S = 1376: ragged k-blocks
+    (19, 1032, 520, 16, 1, 3, 3, 0.1),     # K/S = 344: an 8-element last step
+    (9, 1032, 256, 8, 2, 2, 1, 0.0),       # K/S = 1032: five k-blocks through four stages
 ]
 
 

@@ -23,7 +23,7 @@ def _gpu():
 
 
 def test_plan_picks_tensor_cores_for_large_ranks():
-    for r, want in [(16, ig.PATH_FMA), (24, ig.PATH_FMA), (32, ig.PATH_MMA), (64, ig.PATH_MMA),
+    for r, want in [(16, ig.PATH_WARP), (24, ig.PATH_WARP), (32, ig.PATH_MMA), (64, ig.PATH_MMA),
                     (128, ig.PATH_MMA)]:
         p = ig.plan_query(ig.make_shape(256, 4096, 4096, r, num_adapters=8))
         assert p["path"] == want, r

@@ -147,7 +147,8 @@ def check_expand_fp32(prob, z_gpu, y_gpu):
     assert np.all(err <= tol), float(np.max(err - tol))
 
 
-@pytest.mark.parametrize("r,path", [(16, ig.PATH_FMA), (64, ig.PATH_MMA), (32, ig.PATH_FMA)])
+@pytest.mark.parametrize("r,path", [(16, ig.PATH_WARP), (64, ig.PATH_MMA), (32, ig.PATH_WARP),
+                                    (24, ig.PATH_WARP)])
 def test_fp32_z_expand(r, path):
     p = synth.make_problem(120, 4096, 520, r, slices=2, L=3, seed=r, none_frac=0.1,
                            device="cuda")
