@@ -83,8 +83,11 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   if (partials) part = (size_t)slots * S * pl->tile_rows * pl->bn * sizeof(float);
   pl->total = align_up(pl->off_partials + part, 256);
 
+  // The fused kernel expands N/S columns per block; past 1024 the two-kernel
+  // path (256-column expand blocks) is faster. Both give the same bits.
   pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_WARP && (r == 8 || r == 16) &&
-              pl->bn == r && S <= 16 && !(sh->flags & IG_FLAG_UNFUSED) &&
+              pl->bn == r && S <= 16 && (N + S - 1) / S <= 1024 &&
+              !(sh->flags & IG_FLAG_UNFUSED) &&
               fused_smem_bytes(pl->bn, pl->Ks, N, S) <= 200 * 1024;
 
   uint64_t h = 1469598103934665603ull;

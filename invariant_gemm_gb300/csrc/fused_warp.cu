@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   constexpr int W = ShrinkGeo<BN>::WARPS;
   constexpr int TB = FusedGeo<BN>::TB;
   constexpr int CU = FusedGeo<BN>::CU;
-  constexpr int kPre = 16;   // y words prefetched per lane
+  constexpr int kPre = 64 / W;   // y words prefetched per lane: 512 columns per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -276,14 +276,14 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
             f32_to_bf16_bits(bf16lo(yv) + d[0]) | (f32_to_bf16_bits(bf16hi(yv) + d[1]) << 16);
     };
     if (!zf32) {
-      // the warp's first kPre blocks, 8 at a time: B operands of all 8, then
-      // their MMAs, then the y updates (the MMA of each block is the one
-      // expand_block_mma issues)
+      // Batches of 8 of the warp's blocks: B operands of all 8, then their
+      // MMAs, then the y updates (the MMA of each block is the one
+      // expand_block_mma issues). The first kPre blocks use the prefetched
+      // y; later batches load the y of the next batch before computing the
+      // current one.
       ExpandFrag<BN> zf;
       zf.load_z(zb, lane);
-#pragma unroll
-      for (int h = 0; h < kPre; h += 8) {
-        if (warp + h * W >= nblk) break;
+      auto batch = [&](int h, const uint32_t (&yq)[8]) {
         uint32_t bq[8][2];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -293,7 +293,32 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
         for (int i = 0; i < 8; ++i) zf.mma(dq[i], bq[i]);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (warp + (h + i) * W < nblk) store(warp + (h + i) * W, ypre[h + i], dq[i]);
+          if (warp + (h + i) * W < nblk) store(warp + (h + i) * W, yq[i], dq[i]);
+      };
+      auto load_y = [&](int h, uint32_t (&yq)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int blk = warp + (h + i) * W;
+          yq[i] = (has_row && blk < nblk) ? *reinterpret_cast<const uint32_t*>(yrow + blk * 8)
+                                          : 0u;
+        }
+      };
+      uint32_t ynext[8];
+      if (warp + kPre * W < nblk) load_y(kPre, ynext);
+#pragma unroll
+      for (int h = 0; h < kPre; h += 8) {
+        if (warp + h * W >= nblk) break;
+        uint32_t yq[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) yq[i] = ypre[h + i];
+        batch(h, yq);
+      }
+      for (int h = kPre; warp + h * W < nblk; h += 8) {
+        uint32_t yq[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) yq[i] = ynext[i];
+        if (warp + (h + 8) * W < nblk) load_y(h + 8, ynext);
+        batch(h, yq);
       }
     } else {
 #pragma unroll
@@ -304,12 +329,12 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
         expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
         store(blk, ypre[i], d);
       }
-    }
-    // blocks past the prefetched ones (more than kPre per warp)
-    for (int blk = warp + kPre * W; blk < nblk; blk += W) {
-      float d[4];
-      expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
-      store(blk, has_row ? *reinterpret_cast<const uint32_t*>(yrow + blk * 8) : 0u, d);
+      // blocks past the prefetched ones (more than kPre per warp)
+      for (int blk = warp + kPre * W; blk < nblk; blk += W) {
+        float d[4];
+        expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
+        store(blk, has_row ? *reinterpret_cast<const uint32_t*>(yrow + blk * 8) : 0u, d);
+      }
     }
   }
   // a copy that never completed: wait for it once more (bounded) before the

@@ -65,9 +65,14 @@ struct PartialRing {
   __device__ __forceinline__ int nsub(const PartialArgs& a, int b) const {
     return (klen(a, b) + 63) / 64;
   }
+  // x rows copied per sub-block: 4 per row gather; a last group holding one
+  // row is copied by a one-row tiled load instead (no repeated rows)
+  __device__ __forceinline__ static int x_rows_copied(int nrows) {
+    return (nrows / 4) * 4 + (nrows % 4 == 1 ? 1 : (nrows % 4 ? 4 : 0));
+  }
   // warp 0: arm stage b % nst for all copies of k-block b
   __device__ __forceinline__ void expect(const PartialArgs& a, int b) const {
-    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * (BN + 4 * ((a.nrows + 3) / 4));
+    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * (BN + x_rows_copied(a.nrows));
     if ((threadIdx.x & 31) == 0) mbar_arrive_expect_tx(&bars[b % nst], bytes);
     __syncwarp();
   }
@@ -89,13 +94,18 @@ struct PartialRing {
     uint8_t* sx = stages + st * kStageBytes;
     const int groups4 = (a.nrows + 3) / 4;
     const int last = a.nrows - 1;
-    // one lane per (sub-block, group of 4 rows); rows past nrows repeat the
-    // last row: loaded, never used
+    // one lane per (sub-block, group of 4 rows); in a group of 2 or 3 rows
+    // the last row repeats (loaded, never used); a group of one row is one
+    // tiled copy of that row
     if (lane < nsub(a, b) * groups4) {
       const int q = lane / groups4, gq = lane % groups4;
-      tma_gather4(sx + q * 1024 + gq * 512, a.tm_x, a.k0 + b * kShrinkKB + q * 64,
-                  a.rows[min(4 * gq, last)], a.rows[min(4 * gq + 1, last)],
-                  a.rows[min(4 * gq + 2, last)], a.rows[min(4 * gq + 3, last)], &bars[st]);
+      uint8_t* dst = sx + q * 1024 + gq * 512;
+      const int kc = a.k0 + b * kShrinkKB + q * 64;
+      if (4 * gq == last)
+        tma_load_2d(dst, a.tm_x, kc, a.rows[last], &bars[st]);
+      else
+        tma_gather4(dst, a.tm_x, kc, a.rows[4 * gq], a.rows[min(4 * gq + 1, last)],
+                    a.rows[min(4 * gq + 2, last)], a.rows[min(4 * gq + 3, last)], &bars[st]);
     }
   }
 

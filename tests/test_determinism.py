@@ -291,7 +291,7 @@ FUSED_CASES = [
     (77, 4096, 264, 16, 3, 5, 8, 0.2),     # ragged columns per block, QKV slices
     (256, 4096, 4096, 16, 1, 8, 8, 0.05),
     (40, 512, 512, 8, 1, 1, 8, 0.0),
-    (33, 2048, 1024, 16, 1, 4, 1, 0.0),    # cluster of one
+    (33, 2048, 1024, 16, 1, 4, 1, 0.0),    # cluster of one, 1024 columns per block
     (33, 2048, 1024, 16, 1, 4, 2, 0.0),
     (64, 8192, 1024, 16, 2, 4, 16, 0.1),   # 16-block clusters
     (300, 11008, 4096, 8, 1, 6, 8, 0.0),   # K/S = 1376: ragged k-blocks
