@@ -161,7 +161,7 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
                    uint8_t* ws, cudaStream_t st) {
   MmaExpandParams p;
   int rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N,
-                         (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, kMmaExpandCols,
+                         (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, kMmaExpandBN,
                          CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_y, y, (uint64_t)sh->M, (uint64_t)sh->slices * sh->N,
@@ -362,7 +362,7 @@ int ig_plan_query(const ig_shape* shape, ig_plan_info* out) {
   out->shrink_bm = pl.tile_rows;
   out->shrink_bn = pl.bn;
   out->expand_bm = pl.tile_rows;
-  out->expand_bn = kExpandBN;
+  out->expand_bn = pl.path == IG_PATH_MMA ? kMmaExpandCols : kExpandBN;
   out->shrink_tiles_max = pl.tiles;
   out->shrink_ctas_max = pl.tiles * shape->slices * pl.jblocks * pl.S;
   out->workspace_bytes = (int64_t)pl.total;

@@ -7,19 +7,19 @@
 // and sec. 6.2 / Fig. 5 (the FP32 shrink output reaches the next operation as
 // BF16, rounded to nearest).
 //
-// Block = 4 warps, tile = up to 128 token rows of one adapter (128-row tile
-// table) x 128 output columns of one slice (64 KB of shared memory at r = 64,
-// so that three blocks share an SM and overlap their copies and epilogues). The A operand of the MMA is the
-// tile's Z rows rounded to bf16, written by the threads straight into the
-// 128-byte-swizzled K-major layout; the B operand is B_i's 128 rows x r,
-// brought by tiled TMA copies (64 rank columns each; columns past r read as
-// zero). The y tile (128 rows x 128 columns) is copied by TMA (one box per 64
-// columns when the tile's tokens are consecutive, else row gathers) into
-// swizzled shared memory while the MMA runs. tcgen05.mma, M = 128, N = 128,
-// K = 16 per instruction, r/16 of them,
-// FP32 in tensor memory. Each thread then reads its row of the accumulator,
-// adds it to y in FP32 and rounds once to bf16 in shared memory; a final pass
-// writes y back with whole rows per warp.
+// Block = 4 warps, work = one 128-row tile of one adapter (128-row tile
+// table) x one slice x up to 1024 output columns, streamed as 16 column
+// blocks of 64. The A operand of the MMA, the tile's Z rows rounded to bf16,
+// is built once per block (coalesced loads, written by the threads straight
+// into the 128-byte-swizzled K-major layout) and serves all 16 column
+// blocks. Per column block: the B operand (64 rows of B_i x r) and the y tile
+// (128 rows x 64 columns: one box when the tile's tokens are consecutive,
+// else row gathers) come by TMA into one of two stages, so the copies of
+// block i+2 are in flight while block i is computed; tcgen05.mma, M = 128,
+// N = 64, K = 16 per instruction, r/16 of them, FP32 into one of two TMEM
+// accumulators. Each thread then reads its row of the accumulator, adds it to
+// y in FP32 and rounds once to bf16 in shared memory; the tile goes back by
+// one TMA store when it is 128 consecutive tokens, else by whole-row stores.
 //
 // Arithmetic, fixed by r: the tensor core's FP32 sum over j, then
 // bf16_rn(f32(y) + sum). A row's value depends only on that row.
@@ -30,45 +30,67 @@ namespace ig {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kBN = kMmaExpandCols;              // output columns per block (128)
-constexpr int kYBlocks = kBN / 64;               // 64-column blocks of the y tile
-constexpr int kYBlockBytes = kMmaTileRows * 128; // one 64-column block of the y tile
+constexpr int kBN = kMmaExpandBN;                // output columns per column block
+constexpr int kChunk = kMmaExpandCols;           // output columns per thread block
+constexpr int kNB = kChunk / kBN;                // column blocks per thread block
+constexpr int kYBytes = kMmaTileRows * 128;      // y tile of one column block (16 KB)
+constexpr int kBAtom = kBN * 128;                // B rows of one column block, per 64 ranks
+
+constexpr int kMaxStages = 3;
 
 struct Ctl {
-  uint64_t bar_b;   // B copies
-  uint64_t bar_y;   // y copies
-  uint64_t done;    // MMAs
+  uint64_t full_b[kMaxStages];   // B copies of a stage
+  uint64_t full_y[kMaxStages];   // y copies of a stage
+  uint64_t done[2];              // MMAs of an accumulator
   uint32_t tmem;
-  int32_t fail;     // the B copies never arrived
+  int32_t fail;                  // a B copy never arrived
 };
 
-// layout (offsets from the 1024-aligned base): ctl 1024, tile entry 1024,
-// then zb [r/64][128 rows][128 B], B [r/64][128 rows][128 B], y [2][128][128 B]
-constexpr int kBAtomBytes = kBN * 128;
-// (with FP32 Z: zb holds the hi atoms, then the lo atoms)
-__host__ __device__ inline size_t off_zb() { return 2048; }
-__host__ __device__ inline size_t off_b(int r, bool zf32) {
-  return off_zb() + (size_t)((r + 63) / 64) * 16384 * (zf32 ? 2 : 1);
+// Copy stages. Two: a third stage costs the third block per SM at r = 64,
+// which measured slower (84 us against 52.5 us on the QKV prefill shape).
+__host__ __device__ inline int expand_stages(int) { return 2; }
+
+// layout (offsets from the 1024-aligned base): ctl 0, tile entry 128,
+// zb [parts][r/64][128 rows][128 B] at 1024, then the stages, each
+// {B [r/64][64 rows][128 B], y [128 rows][128 B]}
+__host__ __device__ inline size_t off_zb() { return 1024; }
+__host__ __device__ inline size_t stage_bytes(int r) {
+  return (size_t)((r + 63) / 64) * kBAtom + kYBytes;
 }
-__host__ __device__ inline size_t off_y(int r, bool zf32) {
-  return off_b(r, zf32) + (size_t)((r + 63) / 64) * kBAtomBytes;
+__host__ __device__ inline size_t off_stage(int r, bool zf32, int s) {
+  return off_zb() + (size_t)((r + 63) / 64) * 16384 * (zf32 ? 2 : 1) + s * stage_bytes(r);
 }
 __host__ __device__ inline size_t mma_expand_smem(int r, bool zf32) {
-  return 1024 + off_y(r, zf32) + kYBlocks * kYBlockBytes;
+  return 1024 + off_stage(r, zf32, expand_stages(r));
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1,
+                                             const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+template <int NS>
 __global__ void __launch_bounds__(kThreads)
     expand_mma_kernel(const __grid_constant__ MmaExpandParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
-  int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 1024);
+  int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 128);
   const int r = (int)p.r;
   const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
+  const int ka = (r + 63) / 64;                       // 64-column atoms of the rank
   uint8_t* s_zb = smem + off_zb();
-  uint8_t* s_b = smem + off_b(r, zf32);
-  uint8_t* s_y = smem + off_y(r, zf32);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int64_t bid = blockIdx.x;
@@ -79,14 +101,16 @@ __global__ void __launch_bounds__(kThreads)
 
   for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
   if (tid == 0) {
-    mbar_init(&ctl->bar_b, 1);
-    mbar_init(&ctl->bar_y, 1);
-    mbar_init(&ctl->done, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&ctl->full_b[i], 1);
+      mbar_init(&ctl->full_y[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&ctl->done[i], 1);
     ctl->fail = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem, kBN);
+    tmem_alloc(&ctl->tmem, 2 * kBN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -99,7 +123,7 @@ __global__ void __launch_bounds__(kThreads)
   auto teardown = [&]() {
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, kBN);
+    if (warp == 1) tmem_dealloc(tmem, 2 * kBN);
   };
   if (g < 0 || g >= p.L || nrows <= 0) {
     teardown();
@@ -107,154 +131,214 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   const int64_t N = p.N, M = p.M;
-  const int64_t n0 = (int64_t)nt * kBN;
-  const int ka = (r + 63) / 64;                       // 64-column atoms of the rank
+  const int64_t n0 = (int64_t)nt * kChunk;
+  const int nb = (int)min((int64_t)kNB, (N - n0 + kBN - 1) / kBN);   // column blocks here
   const int b_row = (int)(((int64_t)g * p.slices + sl) * N + n0);
   const int y_col = (int)((int64_t)sl * N + n0);
   const int groups4 = (nrows + 3) / 4;
   const bool contiguous = ent_s[2] != 0;   // rows are consecutive tokens: one box
+  const bool full_box = contiguous && nrows == kMmaTileRows;
   const bool early_b = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
+  const uint32_t y_tx = contiguous ? (uint32_t)kYBytes : (uint32_t)groups4 * 4 * 128;
 
-  auto issue_b = [&]() {
+  // column block i: stage i % NS (phase (i / NS) & 1), accumulator i % 2
+  // (phase (i / 2) & 1)
+  auto stage = [&](int i) { return smem + off_stage(r, zf32, i % NS); };
+  auto sph = [&](int i) { return (uint32_t)((i / NS) & 1); };
+  auto issue_b = [&](int i) {   // thread 0
+    mbar_arrive_expect_tx(&ctl->full_b[i % NS], (uint32_t)ka * kBAtom);
     for (int a = 0; a < ka; ++a)
-      tma_load_2d(s_b + a * kBAtomBytes, &p.tm_b, a * 64, b_row, &ctl->bar_b);
+      tma_load_2d(stage(i) + a * kBAtom, &p.tm_b, a * 64, b_row + i * kBN, &ctl->full_b[i % NS]);
   };
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&ctl->bar_b, (uint32_t)ka * kBAtomBytes);
-    mbar_arrive_expect_tx(&ctl->bar_y, contiguous ? (uint32_t)kYBlocks * kYBlockBytes
-                                                  : (uint32_t)groups4 * 4 * 128 * kYBlocks);
-    if (early_b) issue_b();
-  }
+  auto issue_y = [&](int i) {   // warp 0
+    uint8_t* sy = stage(i) + ka * kBAtom;
+    if (lane == 0) mbar_arrive_expect_tx(&ctl->full_y[i % NS], y_tx);
+    __syncwarp();
+    if (contiguous) {
+      if (lane == 0) tma_load_2d(sy, &p.tm_yt, y_col + i * kBN, rows_s[0], &ctl->full_y[i % NS]);
+      return;
+    }
+    const int last = nrows - 1;
+    for (int q = lane; q < groups4; q += 32)
+      tma_gather4(sy + q * 512, &p.tm_y, y_col + i * kBN, rows_s[min(4 * q, last)],
+                  rows_s[min(4 * q + 1, last)], rows_s[min(4 * q + 2, last)],
+                  rows_s[min(4 * q + 3, last)], &ctl->full_y[i % NS]);
+  };
+
+  if (tid == 0 && early_b)
+    for (int i = 0; i < min(nb, NS); ++i) issue_b(i);
   griddep_wait();
   griddep_launch();
-  if (tid == 0 && !early_b) issue_b();
-  // y tile: 64-column blocks, each one box (consecutive tokens) or row
-  // gathers spread over the lanes of warp 0
-  if (warp == 0 && contiguous) {
-    if (lane < kYBlocks)
-      tma_load_2d(s_y + lane * kYBlockBytes, &p.tm_yt, y_col + lane * 64, rows_s[0], &ctl->bar_y);
-  } else if (warp == 0) {
-    const int last = nrows - 1;
-    for (int q = lane; q < groups4 * kYBlocks; q += 32) {
-      const int cb = q / groups4, g4 = q % groups4;
-      tma_gather4(s_y + cb * kYBlockBytes + g4 * 512, &p.tm_y, y_col + cb * 64,
-                  rows_s[min(4 * g4, last)], rows_s[min(4 * g4 + 1, last)],
-                  rows_s[min(4 * g4 + 2, last)], rows_s[min(4 * g4 + 3, last)], &ctl->bar_y);
+  if (warp == 0) {
+    for (int i = 0; i < min(nb, NS); ++i) {
+      if (lane == 0 && !early_b) issue_b(i);
+      issue_y(i);
     }
   }
 
-  // A operand: this thread's Z row (token row `tid` of the tile), rounded to
-  // bf16, into the swizzled K-major layout (16-byte chunk c of a 128-byte row
-  // m sits at chunk c ^ (m % 8)). With FP32 Z also the remainder
+  // A operand: the tile's Z rows rounded to bf16 into the swizzled K-major
+  // layout (16-byte chunk c of a 128-byte row m sits at chunk c ^ (m % 8)),
+  // rows past nrows zero. Warp w loads rows 32w .. 32w+31, r/4 lanes per row
+  // (4 values each, coalesced). With FP32 Z also the remainder
   // lo = bf16_rn(z - hi), in atoms after the hi ones.
   {
-    const int m = tid;
-    const bool valid = m < nrows;
-    const float* zr = p.z + ((int64_t)sl * M + (valid ? rows_s[m] : 0)) * r;
-    for (int a = 0; a < ka; ++a) {
-      uint8_t* rowp = s_zb + a * 16384 + m * 128;
-      uint8_t* lowp = s_zb + (ka + a) * 16384 + m * 128;
+    const int per_row = r / 4;
+    for (int idx = lane; idx < 32 * per_row; idx += 32) {
+      const int m = warp * 32 + idx / per_row;
+      const int j = 4 * (idx % per_row);
+      float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (m < nrows) f = __ldcg(reinterpret_cast<const float4*>(p.z + ((int64_t)sl * M + rows_s[m]) * r + j));
+      const float fv[4] = {f.x, f.y, f.z, f.w};
+      uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0;
-        if (valid && a * 64 + c * 8 < r) {
-          const float4 f0 = __ldcg(reinterpret_cast<const float4*>(zr + a * 64 + c * 8));
-          const float4 f1 = __ldcg(reinterpret_cast<const float4*>(zr + a * 64 + c * 8 + 4));
-          const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            hi[e] = f32_to_bf16_bits(f[e]);
-            if (zf32) lo[e] = f32_to_bf16_bits(f[e] - __uint_as_float(hi[e] << 16));
-          }
-        }
-        const int pc = (c ^ (m & 7)) * 16;
-        *reinterpret_cast<uint4*>(rowp + pc) = make_uint4(
-            hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16), hi[6] | (hi[7] << 16));
-        if (zf32)
-          *reinterpret_cast<uint4*>(lowp + pc) = make_uint4(
-              lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16), lo[4] | (lo[5] << 16), lo[6] | (lo[7] << 16));
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = f32_to_bf16_bits(fv[e]);
+        lo[e] = zf32 ? f32_to_bf16_bits(fv[e] - __uint_as_float(hi[e] << 16)) : 0u;
+      }
+      const int a = j / 64, c = (j % 64) / 8;
+      const size_t off = (size_t)a * 16384 + m * 128 + ((c ^ (m & 7)) << 4) + (j % 8) * 2;
+      *reinterpret_cast<uint2*>(s_zb + off) = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+      if (zf32)
+        *reinterpret_cast<uint2*>(s_zb + (size_t)ka * 16384 + off) =
+            make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+    }
+    // rank columns past r inside the last atom are zero
+    if (r % 64) {
+      for (int idx = tid; idx < kMmaTileRows * ((64 - r % 64) / 8); idx += kThreads) {
+        const int m = idx / ((64 - r % 64) / 8);
+        const int c = (r % 64) / 8 + idx % ((64 - r % 64) / 8);
+        const size_t off = (size_t)(ka - 1) * 16384 + m * 128 + ((c ^ (m & 7)) << 4);
+        *reinterpret_cast<uint4*>(s_zb + off) = make_uint4(0u, 0u, 0u, 0u);
+        if (zf32) *reinterpret_cast<uint4*>(s_zb + (size_t)ka * 16384 + off) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
   fence_proxy_async_smem();
   __syncthreads();
 
-  if (warp == 1 && lane == 0) {
-    if (mbar_wait_bounded(&ctl->bar_b, 0, p.status)) {
+  const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, kBN);
+  // MMAs of column block i into accumulator i % 2 (thread 32); the B copy
+  // of the block has been waited for, or the wait is bounded here
+  auto issue_mma = [&](int i, bool b_ready) {
+    const uint32_t acc = tmem + (uint32_t)((i & 1) * kBN);
+    if (b_ready || mbar_wait_bounded(&ctl->full_b[i % NS], sph(i), p.status)) {
       tc_fence_after();
-      const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, kBN);
+      const uint32_t sb = smem_u32(stage(i));
       for (int k = 0; k < r / 16; ++k) {
         const int a = k / 4, kk = k % 4;
-        const uint64_t bdesc = umma_desc_sw128(smem_u32(s_b + a * kBAtomBytes) + kk * 32);
-        umma_bf16(tmem, umma_desc_sw128(smem_u32(s_zb + a * 16384) + kk * 32), bdesc, idesc,
+        const uint64_t bdesc = umma_desc_sw128(sb + a * kBAtom + kk * 32);
+        umma_bf16(acc, umma_desc_sw128(smem_u32(s_zb + a * 16384) + kk * 32), bdesc, idesc,
                   k > 0);
         if (zf32)
-          umma_bf16(tmem, umma_desc_sw128(smem_u32(s_zb + (ka + a) * 16384) + kk * 32), bdesc,
+          umma_bf16(acc, umma_desc_sw128(smem_u32(s_zb + (ka + a) * 16384) + kk * 32), bdesc,
                     idesc, true);
       }
     } else {
       ctl->fail = 1;
     }
-    umma_commit(&ctl->done);
-  }
-  __syncwarp();
-  const bool y_ok = mbar_wait_bounded(&ctl->bar_y, 0, p.status);
-  const bool acc_ok = mbar_wait_bounded(&ctl->done, 0, p.status) &&
-                      *reinterpret_cast<volatile int32_t*>(&ctl->fail) == 0;
-  tc_fence_after();
+    umma_commit(&ctl->done[i & 1]);
+  };
+  int next_mma = 0;   // thread 32: first block whose MMAs are not issued yet
+  if (tid == 32) issue_mma(next_mma++, false);
 
-  // epilogue 1: this thread's row: y = bf16_rn(f32(y) + acc), in shared memory
-  {
-    const int m = tid;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int c = 0; c < kBN; c += 32) {
-      float v[32];
-      tmem_ld32(trow + c, v);
-      if (!(acc_ok && y_ok) || m >= nrows) continue;
-      const int cb = c / 64;
-      uint8_t* rowp = s_y + cb * kYBlockBytes + m * 128;
+  const int64_t ld = (int64_t)p.slices * N;
+  int issued = min(nb, NS);   // column blocks whose copies have been issued
+  int i = 0;
+  bool ok = true;
+  for (; i < nb; ++i) {
+    // the next block's MMAs overlap this block's epilogue (other
+    // accumulator) when its B copy is already there; else they follow the
+    // epilogue
+    if (tid == 32 && next_mma == i + 1 && next_mma < nb &&
+        mbar_try_wait(&ctl->full_b[next_mma % NS], sph(next_mma)))
+      issue_mma(next_mma++, true);
+    __syncwarp();
+    const bool y_ok = mbar_wait_bounded(&ctl->full_y[i % NS], sph(i), p.status);
+    const bool acc_ok = mbar_wait_bounded(&ctl->done[i & 1], (uint32_t)((i >> 1) & 1), p.status) &&
+                        *reinterpret_cast<volatile int32_t*>(&ctl->fail) == 0;
+    tc_fence_after();
+    if (__syncthreads_or(!(y_ok && acc_ok))) {
+      ok = false;
+      break;
+    }
+    uint8_t* sy = stage(i) + ka * kBAtom;
+
+    // epilogue 1: this thread's row: y = bf16_rn(f32(y) + acc), in shared memory
+    {
+      const int m = tid;
+      const uint32_t trow = tmem + (uint32_t)((i & 1) * kBN) + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = ((c % 64) / 8) + q;            // logical 16-byte chunk in the row
-        uint4* cp = reinterpret_cast<uint4*>(rowp + ((chunk ^ (m & 7)) * 16));
-        uint4 u = *cp;
-        float yf[8];
-        unpack8(u, yf);
-        uint32_t o[8];
+      for (int c = 0; c < kBN; c += 32) {
+        float v[32];
+        tmem_ld32(trow + c, v);
+        if (m >= nrows) continue;
+        uint8_t* rowp = sy + m * 128;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = f32_to_bf16_bits(yf[e] + v[8 * q + e]);
-        u.x = o[0] | (o[1] << 16);
-        u.y = o[2] | (o[3] << 16);
-        u.z = o[4] | (o[5] << 16);
-        u.w = o[6] | (o[7] << 16);
-        *cp = u;
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = c / 8 + q;                       // logical 16-byte chunk
+          uint4* cp = reinterpret_cast<uint4*>(rowp + ((chunk ^ (m & 7)) * 16));
+          uint4 u = *cp;
+          float yf[8];
+          unpack8(u, yf);
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = f32_to_bf16_bits(yf[e] + v[8 * q + e]);
+          u.x = o[0] | (o[1] << 16);
+          u.y = o[2] | (o[3] << 16);
+          u.z = o[4] | (o[5] << 16);
+          u.w = o[6] | (o[7] << 16);
+          *cp = u;
+        }
       }
     }
-  }
-  __syncthreads();
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncthreads();
 
-  // epilogue 2: two whole rows (256 bytes each) per warp-instruction back to
-  // global memory
-  if (acc_ok && y_ok) {
-    const int64_t ld = (int64_t)p.slices * N;
-    const int64_t ncols = min((int64_t)kBN, N - n0);
-    for (int m0 = 2 * warp; m0 < nrows; m0 += 8) {
-      const int m = m0 + lane / 16;
-      const int ch = lane % 16;            // 16-byte chunk of the 256-byte row
-      if (m >= nrows || (int64_t)ch * 8 >= ncols) continue;
-      const int cb = ch / 8, c = ch % 8;
-      const uint4 u =
-          *reinterpret_cast<const uint4*>(s_y + cb * kYBlockBytes + m * 128 + ((c ^ (m & 7)) * 16));
-      *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[m] * ld + y_col + ch * 8) = u;
+    // epilogue 2: back to global memory
+    const int ncols = (int)min((int64_t)kBN, N - n0 - (int64_t)i * kBN);
+    if (full_box && ncols == kBN) {
+      if (tid == 0) {
+        tma_store_2d(&p.tm_yt, y_col + i * kBN, rows_s[0], sy);
+        bulk_commit();
+      }
+    } else {
+      // four rows (128 bytes each) per warp-instruction
+      for (int m0 = 4 * warp; m0 < nrows; m0 += 16) {
+        const int m = m0 + lane / 8;
+        const int ch = lane % 8;              // 16-byte chunk of the 128-byte row
+        if (m >= nrows || ch * 8 >= ncols) continue;
+        const uint4 u = *reinterpret_cast<const uint4*>(sy + m * 128 + ((ch ^ (m & 7)) * 16));
+        *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + ch * 8) = u;
+      }
     }
+    __syncthreads();
+    // stage i % NS is free once the store has read it: copies of block i + NS
+    if (i + NS < nb) {
+      if (warp == 0) {
+        if (lane == 0) {
+          bulk_wait_read0();
+          issue_b(i + NS);
+        }
+        __syncwarp();
+        issue_y(i + NS);
+      }
+      issued = i + NS + 1;
+    }
+    if (tid == 32 && next_mma == i + 1 && next_mma < nb) issue_mma(next_mma++, false);
   }
-  if (!(acc_ok && y_ok)) {
-    if (tid == 0) {
-      mbar_wait_bounded(&ctl->bar_b, 0, p.status);
-      mbar_wait_bounded(&ctl->bar_y, 0, p.status);
-    }
+  if (tid == 0) bulk_wait_read0();
+  if (!ok) {
+    // drain (bounded) what may still be in flight before the block leaves:
+    // the copies of blocks i .. issued-1 and the MMAs issued for blocks >= i
+    if (tid == 0)
+      for (int b = i; b < issued; ++b) {
+        mbar_wait_bounded(&ctl->full_b[b % NS], sph(b), p.status);
+        mbar_wait_bounded(&ctl->full_y[b % NS], sph(b), p.status);
+      }
+    if (tid == 32)
+      for (int b = i; b < next_mma; ++b)
+        mbar_wait_bounded(&ctl->done[b & 1], (uint32_t)((b >> 1) & 1), p.status);
   }
   teardown();
 }
@@ -263,13 +347,14 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st) {
   const size_t smem = mma_expand_smem((int)p.r, (p.flags & IG_FLAG_Z_FP32) != 0);
-  cudaError_t e = cudaFuncSetAttribute(expand_mma_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  void (*kern)(MmaExpandParams) =
+        expand_stages((int)p.r) == 3 ? expand_mma_kernel<3> : expand_mma_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = tiles_max * p.slices * p.ntiles;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  return launch_pdl(expand_mma_kernel, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
 }
 
 size_t expand_mma_smem_bytes(int r) { return mma_expand_smem(r, false); }

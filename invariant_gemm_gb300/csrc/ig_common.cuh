@@ -55,7 +55,8 @@ constexpr int kArithRevision = 2;
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
-constexpr int kMmaExpandCols = 128;    // output columns per tensor-core expand block
+constexpr int kMmaExpandCols = 1024;   // output columns per tensor-core expand block
+constexpr int kMmaExpandBN = 64;       // output columns per MMA (N) of that block
 
 // Tile count over token groups: sum over groups g of ceil(count_g / bm),
 // bounded by floor(M / bm) + (number of non-empty groups).
@@ -152,7 +153,7 @@ struct MmaShrinkParams {
 };
 
 struct MmaExpandParams {
-  CUtensorMap tm_b;     // B_stack as [L*slices*N][r], box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_b;     // B_stack as [L*slices*N][r], box 64 x 64, 128-byte swizzle
   CUtensorMap tm_y;     // y [M][slices*N], box 64 x 1, 128-byte swizzle (row gathers)
   CUtensorMap tm_yt;    // y [M][slices*N], box 64 x 128, 128-byte swizzle (contiguous tiles)
   const float* z;
