@@ -39,33 +39,6 @@ namespace ig {
 
 namespace {
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Split cluster barrier. The arrive carries no memory ordering: it only
-// tells the other blocks that this block's mbarriers are initialised (made
-// visible to the cluster by fence.mbarrier_init before it).
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-// Address of the same shared-memory offset in block `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_rank(const void* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  return remote;
-}
-// Asynchronous 4-byte store into another block's shared memory; its bytes
-// are counted (complete_tx) on that block's mbarrier `remote_bar`.
-__device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
-               ::"r"(remote), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
-}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

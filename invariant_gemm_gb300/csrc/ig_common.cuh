@@ -285,6 +285,49 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// --- thread-block clusters ------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Split cluster barrier. The arrive carries no memory ordering: it only
+// tells the other blocks that this block's mbarriers are initialised (made
+// visible to the cluster by fence.mbarrier_init before it).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+// Asynchronous 4-byte store into another block's shared memory; its bytes
+// are counted (complete_tx) on that block's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(remote), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
+}
+// Asynchronous 16-byte store into another block's shared memory, counted on
+// that block's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t remote, float4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(remote), "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)),
+        "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w)), "r"(remote_bar) : "memory");
+}
+// Full cluster barrier: every block's earlier memory operations are visible
+// to the cluster afterwards.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Tiled 2-D tensor copy global -> shared (box of the tensor map at
 // coordinates {c0 = column, c1 = row}); c0 * 2 bytes must be a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,

@@ -14,6 +14,15 @@
 //   sec. 4.2        UNSPLIT: S = 1;
 //   sec. 4.3        DET_TREE: partials only, combined by reduce_tree.cu.
 //
+// DET with S dividing 128 and S <= 16 (when such a cluster can be resident):
+// the S blocks of a tile are one thread-block cluster. After a cluster
+// barrier (every block's MMAs done, its copy ring free), block s owns tile
+// rows [s 128/S, (s+1) 128/S): every thread sends its accumulator row to the
+// owner with asynchronous remote stores counted on the owner's mbarrier, and
+// the owner sums the S partials of its rows from FP32 zero in increasing
+// partition order and scales them: the counter protocol's order, so the same
+// bits, with the partials never leaving the SMs.
+//
 // Block = 4 warps, tile = up to 128 token rows of one adapter (one entry of
 // the token map's 128-row tile table) x all r rank columns. One thread of
 // warp 0 issues the TMA copies: per k-step of 64 elements, x as one 128-row
@@ -30,6 +39,10 @@
 // accumulation of the K-steps in order within the partition, then the
 // partitions summed in increasing order. A row's value depends only on that
 // row, its adapter and the plan.
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "umma.cuh"
 
 namespace ig {
@@ -45,6 +58,7 @@ struct Ctl {                       // control block at the start of shared memor
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t done;
+  uint64_t recv;                   // cluster combine: partial rows received
   uint32_t tmem;
   int32_t info[4];
 };
@@ -60,7 +74,9 @@ __host__ __device__ inline uint32_t tmem_cols_for(int r) {
   return c;
 }
 
-template <int MODE>
+// CL (IG_MODE_DET only): the S partition blocks of a tile are one cluster and
+// combine there instead of through scratch and the counter.
+template <int MODE, bool CL>
 __global__ void __launch_bounds__(kThreads)
     shrink_mma_kernel(const __grid_constant__ MmaShrinkParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -88,6 +104,7 @@ __global__ void __launch_bounds__(kThreads)
       mbar_init(&ctl->empty[i], 1);
     }
     mbar_init(&ctl->done, 1);
+    if (CL) mbar_init(&ctl->recv, 1);
     fence_mbar_init();
   }
   const uint32_t ncols = tmem_cols_for(r);
@@ -103,6 +120,11 @@ __global__ void __launch_bounds__(kThreads)
   const int nrows = ent_s[1];
   const int32_t* rows_s = ent_s + 4;
   const int64_t M = p.M;
+  // cluster combine: block s owns tile rows [s R, s R + R), R = 128 / S, and
+  // receives the S partials of its valid rows
+  const int R = kMmaTileRows / S;
+  const int own_rows = max(0, min(R, nrows - s * R));
+  if (CL && tid == 0) mbar_arrive_expect_tx(&ctl->recv, (uint32_t)(S * own_rows * r * 4));
 
   auto teardown = [&]() {
     tc_fence_before();
@@ -206,6 +228,57 @@ __global__ void __launch_bounds__(kThreads)
   tc_fence_after();
   const int row = warp * 32 + lane;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  if (CL) {
+    // Every block's MMAs are complete (so its ring is free) once the cluster
+    // barrier returns. Each thread then sends its accumulator row to the
+    // owner of the row, into slot s of the owner's receive buffer
+    // [S][R][r] FP32 (the ring), counted on the owner's mbarrier. Every block
+    // sends on every path, so every owner receives all its bytes.
+    fence_proxy_async_smem();
+    cluster_sync_all();
+    float* recv = reinterpret_cast<float*>(ring);
+    const int q = row / R, lr = row % R;
+    const uint32_t dst_bar = map_rank(&ctl->recv, (uint32_t)q);
+    for (int c = 0; c < r; c += 32) {
+      float v[32];
+      tmem_ld32(trow + c, v);
+      if (row >= nrows) continue;
+      const int nv = min(32, r - c);   // r is a multiple of 16
+      const uint32_t dst = map_rank(recv + ((size_t)s * R + lr) * r + c, (uint32_t)q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (4 * i < nv)
+          st_async_v4(dst + 16 * i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]),
+                      dst_bar);
+    }
+    // The wait outlasts any sender's bounded waits, so the block never leaves
+    // while a partial is still on its way to it.
+    const bool got = mbar_wait_bounded(&ctl->recv, 0, p.status, 1ll << 36);
+    // Combine (Algorithm 1 order) of the owned rows: total = 0; total += P_q
+    // for q = 0..S-1; z = total * scale. Four columns per step.
+    const int n4 = own_rows * r / 4;
+    const float4* rv = reinterpret_cast<const float4*>(recv);
+    for (int o4 = tid; got && acc_ok && o4 < n4; o4 += kThreads) {
+      float4 total = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int q2 = 0; q2 < S; ++q2) {
+        const float4 v = rv[q2 * (R * r / 4) + o4];
+        total.x += v.x;
+        total.y += v.y;
+        total.z += v.z;
+        total.w += v.w;
+      }
+      const int o = 4 * o4;
+      *reinterpret_cast<float4*>(p.z + ((int64_t)sl * M + rows_s[s * R + o / r]) * r + o % r) =
+          make_float4(total.x * p.scale, total.y * p.scale, total.z * p.scale,
+                      total.w * p.scale);
+    }
+    if (failed || !acc_ok) {
+      if (tid == 0)
+        for (int st = 0; st < kStages; ++st) mbar_wait_bounded(&ctl->full[st], 0, p.status);
+    }
+    teardown();
+    return;
+  }
   const int64_t slot = t * p.slices + sl;
   float* part = p.partials + slot * (int64_t)S * (kMmaTileRows * r);
   for (int c = 0; c < r; c += 32) {
@@ -298,7 +371,7 @@ __global__ void __launch_bounds__(kThreads)
 
 template <int MODE>
 cudaError_t launch_mode(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
-  auto kern = shrink_mma_kernel<MODE>;
+  auto kern = shrink_mma_kernel<MODE, false>;
   const size_t smem = mma_shrink_smem((int)p.r);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -309,11 +382,85 @@ cudaError_t launch_mode(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
 }
 
+// Can a cluster of S blocks of this size be resident? Cached per (S, r).
+bool cluster_fits(int S, int r) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, bool> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(S, r);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  auto kern = shrink_mma_kernel<IG_MODE_DET, true>;
+  const size_t smem = mma_shrink_smem(r);
+  bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) == cudaSuccess;
+  if (ok && S > 8)
+    ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+         cudaSuccess;
+  int n = 0;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ok = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
+  }
+  cudaGetLastError();   // clear a refused query
+  cache[key] = ok;
+  return ok;
+}
+
+cudaError_t launch_cluster(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
+  auto kern = shrink_mma_kernel<IG_MODE_DET, true>;
+  const size_t smem = mma_shrink_smem((int)p.r);
+  // per launch: the attribute is per function, and other ranks set it too
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  if (p.S > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t grid = tiles_max * p.slices * p.S;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
                               cudaStream_t st) {
-  if (mode == IG_MODE_DET) return launch_mode<IG_MODE_DET>(p, tiles_max, st);
+  if (mode == IG_MODE_DET) {
+    // the cluster combine and the counter protocol give the same bits
+    // (rows are dealt to the S blocks in equal shares: S must divide 128)
+    if (p.S <= 16 && kMmaTileRows % p.S == 0 && cluster_fits(p.S, (int)p.r))
+      return launch_cluster(p, tiles_max, st);
+    return launch_mode<IG_MODE_DET>(p, tiles_max, st);
+  }
   if (mode == IG_MODE_DET_TREE) return launch_mode<IG_MODE_DET_TREE>(p, tiles_max, st);
   if (mode == IG_MODE_ATOMIC) return launch_mode<IG_MODE_ATOMIC>(p, tiles_max, st);
   return launch_mode<IG_MODE_UNSPLIT>(p, tiles_max, st);
