@@ -127,11 +127,15 @@ typedef struct ig_shape {
                                     weights). Lets a kernel start reading
                                     them while the previous kernel on the
                                     stream is still finishing. */
-#define IG_FLAG_UNFUSED 2        /* lora_apply in IG_MODE_DET runs the Split-K
-                                    shrink (counter protocol, Algorithm 1)
-                                    and the expand as two kernels even where
-                                    the fused one-launch kernel applies. Both
-                                    give the same bits. */
+#define IG_FLAG_UNFUSED 2        /* IG_MODE_DET combines through the
+                                    workspace with the completion counter
+                                    (Algorithm 1) even where a cluster
+                                    combine applies: lora_apply runs the
+                                    Split-K shrink and the expand as two
+                                    kernels instead of the fused one-launch
+                                    kernel, and the tcgen05 shrink does not
+                                    combine inside a thread-block cluster.
+                                    Both give the same bits. */
 #define IG_FLAG_Z_FP32 4         /* The expand reads Z in FP32 instead of
                                     rounding it to bf16 first (sec. 6.2 shows
                                     the bf16 boundary turning tiny FP32

@@ -50,13 +50,20 @@ namespace ig {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
+// Copy ring depth: 4 stages up to r = 64, 3 at r = 128, 2 at r = 256, so that
+// two blocks share an SM (one per SM leaves 16-block clusters short of SMs).
+__host__ __device__ inline int shrink_stages(int r) {
+  const int stage = kMmaTileRows * 128 + r * 128;
+  const int n = (110 * 1024) / stage;
+  return n < 2 ? 2 : (n > kMaxStages ? kMaxStages : n);
+}
 constexpr int kKStep = 64;                      // elements per k-step (128 bytes)
 constexpr int kXTileBytes = kMmaTileRows * 128;  // 16 KB
 
 struct Ctl {                       // control block at the start of shared memory
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t done;
   uint64_t recv;                   // cluster combine: partial rows received
   uint32_t tmem;
@@ -65,7 +72,8 @@ struct Ctl {                       // control block at the start of shared memor
 
 __host__ __device__ inline size_t mma_shrink_smem(int r) {
   const size_t stage = kXTileBytes + (size_t)r * 128;
-  return 1024 /*align slack*/ + 1024 /*ctl*/ + (size_t)kMmaTileInts * 4 + kStages * stage + 1024;
+  return 1024 /*align slack*/ + 1024 /*ctl*/ + (size_t)kMmaTileInts * 4 +
+         (size_t)shrink_stages(r) * stage + 1024;
 }
 
 __host__ __device__ inline uint32_t tmem_cols_for(int r) {
@@ -88,6 +96,7 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* ring = smem + 1024 + ((kMmaTileInts * 4 + 1023) / 1024) * 1024;
   const int r = (int)p.r;
   const int stage_bytes = kXTileBytes + r * 128;
+  const int nst = shrink_stages(r);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
@@ -99,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
 
   for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < nst; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], 1);
     }
@@ -155,23 +164,23 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t stage_tx =
       (contiguous ? (uint32_t)kXTileBytes : (uint32_t)groups4 * 4 * 128) + (uint32_t)r * 128;
   const bool early_a = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
-  const int first = min(nk, kStages);
+  const int first = min(nk, nst);
 
   auto issue_a = [&](int b) {
-    uint8_t* st = ring + (b % kStages) * stage_bytes;
-    tma_load_2d(st + kXTileBytes, &p.tm_a, k0 + b * kKStep, a_row, &ctl->full[b % kStages]);
+    uint8_t* st = ring + (b % nst) * stage_bytes;
+    tma_load_2d(st + kXTileBytes, &p.tm_a, k0 + b * kKStep, a_row, &ctl->full[b % nst]);
   };
   auto issue_x = [&](int b) {
-    uint8_t* st = ring + (b % kStages) * stage_bytes;
+    uint8_t* st = ring + (b % nst) * stage_bytes;
     if (contiguous) {
-      tma_load_2d(st, &p.tm_xt, k0 + b * kKStep, rows_s[0], &ctl->full[b % kStages]);
+      tma_load_2d(st, &p.tm_xt, k0 + b * kKStep, rows_s[0], &ctl->full[b % nst]);
       return;
     }
     const int last = nrows - 1;
     for (int q = 0; q < groups4; ++q)
       tma_gather4(st + q * 4 * 128, &p.tm_x, k0 + b * kKStep, rows_s[min(4 * q, last)],
                   rows_s[min(4 * q + 1, last)], rows_s[min(4 * q + 2, last)],
-                  rows_s[min(4 * q + 3, last)], &ctl->full[b % kStages]);
+                  rows_s[min(4 * q + 3, last)], &ctl->full[b % nst]);
   };
 
   bool failed = false;
@@ -188,8 +197,8 @@ __global__ void __launch_bounds__(kThreads)
     // producer
     for (int b = 0; b < nk; ++b) {
       if (b >= first) {
-        const int st = b % kStages;
-        if (!mbar_wait_bounded(&ctl->empty[st], (uint32_t)(((b / kStages) - 1) & 1), p.status)) {
+        const int st = b % nst;
+        if (!mbar_wait_bounded(&ctl->empty[st], (uint32_t)(((b / nst) - 1) & 1), p.status)) {
           failed = true;
           break;
         }
@@ -204,8 +213,8 @@ __global__ void __launch_bounds__(kThreads)
     // MMA issuer
     const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, r);
     for (int b = 0; b < nk; ++b) {
-      const int st = b % kStages;
-      if (!mbar_wait_bounded(&ctl->full[st], (uint32_t)((b / kStages) & 1), p.status)) {
+      const int st = b % nst;
+      if (!mbar_wait_bounded(&ctl->full[st], (uint32_t)((b / nst) & 1), p.status)) {
         failed = true;
         break;
       }
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (failed || !acc_ok) {
       if (tid == 0)
-        for (int st = 0; st < kStages; ++st) mbar_wait_bounded(&ctl->full[st], 0, p.status);
+        for (int st = 0; st < nst; ++st) mbar_wait_bounded(&ctl->full[st], 0, p.status);
     }
     teardown();
     return;
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kThreads)
   if (failed || !acc_ok) {
     // drain (bounded) the copies of stages that were issued and not consumed
     if (tid == 0)
-      for (int st = 0; st < kStages; ++st)
+      for (int st = 0; st < nst; ++st)
         mbar_wait_bounded(&ctl->full[st], 0, p.status);
   }
   teardown();
@@ -456,8 +465,13 @@ cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_
                               cudaStream_t st) {
   if (mode == IG_MODE_DET) {
     // the cluster combine and the counter protocol give the same bits
-    // (rows are dealt to the S blocks in equal shares: S must divide 128)
-    if (p.S <= 16 && kMmaTileRows % p.S == 0 && cluster_fits(p.S, (int)p.r))
+    // (rows are dealt to the S blocks in equal shares, S must divide 128; the
+    // received partials, 128 rows x r FP32, live in the copy ring)
+    const int r = (int)p.r;
+    const bool recv_fits = (size_t)kMmaTileRows * r * 4 <=
+                           (size_t)shrink_stages(r) * (kXTileBytes + (size_t)r * 128);
+    if (!(p.flags & IG_FLAG_UNFUSED) && p.S <= 16 && kMmaTileRows % p.S == 0 && recv_fits &&
+        cluster_fits(p.S, r))
       return launch_cluster(p, tiles_max, st);
     return launch_mode<IG_MODE_DET>(p, tiles_max, st);
   }

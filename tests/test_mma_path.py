@@ -95,3 +95,21 @@ def test_mma_contiguous_tiles_with_overhang(mode):
     z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
     check_shrink(p.to("cpu"), z)
     check_expand(p.to("cpu"), z, y)
+
+
+@pytest.mark.parametrize("r,K,S", [(32, 2048, 8), (64, 11008, 8), (128, 8192, 16), (64, 4096, 4)])
+def test_mma_cluster_combine_bitwise_equals_counter(r, K, S):
+    """The deterministic tcgen05 shrink combines inside a thread-block cluster
+    where it can; IG_FLAG_UNFUSED forces the counter protocol (Algorithm 1).
+    Same order of the partition sum, so the same bits for z and y."""
+    p = synth.make_problem(300, K, 520, r, slices=2, L=5, seed=r + S, none_frac=0.1,
+                           device="cuda")
+    outs = []
+    for flags in (0, ig.FLAG_UNFUSED):
+        sh = ig.make_shape(p.M, K, p.N, r, slices=2, num_adapters=5, split_k=S,
+                           mode=ig.MODE_DET, path=ig.PATH_MMA, flags=flags)
+        outs.append(run_apply(p, shape=sh))
+    assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32))
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+    check_shrink(p.to("cpu"), outs[0][0])
+    check_expand(p.to("cpu"), outs[0][0], outs[0][1])
