@@ -5,6 +5,9 @@
 #include <cstring>
 #include <mutex>
 
+#include <algorithm>
+#include <map>
+
 #include "ig_common.cuh"
 
 namespace ig {
@@ -100,6 +103,22 @@ int make_plan(const ig_shape* sh, Plan* pl) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// SMs of the current device (cached per device; 152 on GB300).
+int sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 152;
+  cache[dev] = n;
+  return n;
+}
+
 int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
   if (!ws) return IG_ERR_ARG;
   if (!aligned16(ws)) return IG_ERR_ALIGN;
@@ -180,7 +199,14 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
   p.r = sh->r;
   p.slices = sh->slices;
   p.L = sh->num_adapters;
-  p.ntiles = (int)((sh->N + kMmaExpandCols - 1) / kMmaExpandCols);
+  // column blocks of 64 per thread block: enough blocks for about three per
+  // SM, each streaming at least 2 and at most 16 column blocks
+  const int64_t nblk = (sh->N + kMmaExpandBN - 1) / kMmaExpandBN;
+  const int64_t units = pl.tiles * sh->slices * nblk;
+  const int64_t target = 3 * (int64_t)sm_count();
+  p.nb = (int)std::min<int64_t>(kMmaExpandCols / kMmaExpandBN,
+                                std::max<int64_t>(2, (units + target - 1) / target));
+  p.ntiles = (int)((nblk + p.nb - 1) / p.nb);
   p.flags = sh->flags;
   return cuda_status(launch_expand_mma(p, pl.tiles, st));
 }

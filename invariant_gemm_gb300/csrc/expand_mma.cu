@@ -8,10 +8,11 @@
 // BF16, rounded to nearest).
 //
 // Block = 4 warps, work = one 128-row tile of one adapter (128-row tile
-// table) x one slice x up to 1024 output columns, streamed as 16 column
-// blocks of 64. The A operand of the MMA, the tile's Z rows rounded to bf16,
+// table) x one slice x nb column blocks of 64 (2 <= nb <= 16, chosen on the
+// host so that the grid fills the GPU about three blocks per SM; it does not
+// change any result). The A operand of the MMA, the tile's Z rows rounded to bf16,
 // is built once per block (coalesced loads, written by the threads straight
-// into the 128-byte-swizzled K-major layout) and serves all 16 column
+// into the 128-byte-swizzled K-major layout) and serves all its column
 // blocks. Per column block: the B operand (64 rows of B_i x r) and the y tile
 // (128 rows x 64 columns: one box when the tile's tokens are consecutive,
 // else row gathers) come by TMA into one of two stages, so the copies of
@@ -31,8 +32,6 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kBN = kMmaExpandBN;                // output columns per column block
-constexpr int kChunk = kMmaExpandCols;           // output columns per thread block
-constexpr int kNB = kChunk / kBN;                // column blocks per thread block
 constexpr int kYBytes = kMmaTileRows * 128;      // y tile of one column block (16 KB)
 constexpr int kBAtom = kBN * 128;                // B rows of one column block, per 64 ranks
 
@@ -131,8 +130,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   const int64_t N = p.N, M = p.M;
-  const int64_t n0 = (int64_t)nt * kChunk;
-  const int nb = (int)min((int64_t)kNB, (N - n0 + kBN - 1) / kBN);   // column blocks here
+  const int64_t n0 = (int64_t)nt * p.nb * kBN;
+  const int nb = (int)min((int64_t)p.nb, (N - n0 + kBN - 1) / kBN);   // column blocks here
   const int b_row = (int)(((int64_t)g * p.slices + sl) * N + n0);
   const int y_col = (int)((int64_t)sl * N + n0);
   const int groups4 = (nrows + 3) / 4;

@@ -55,7 +55,7 @@ constexpr int kArithRevision = 2;
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
-constexpr int kMmaExpandCols = 1024;   // output columns per tensor-core expand block
+constexpr int kMmaExpandCols = 1024;   // most output columns per tensor-core expand block
 constexpr int kMmaExpandBN = 64;       // output columns per MMA (N) of that block
 
 // Tile count over token groups: sum over groups g of ceil(count_g / bm),
@@ -162,6 +162,7 @@ struct MmaExpandParams {
   uint32_t* status;
   int64_t M, N, r;
   int32_t slices, L, ntiles, flags;
+  int32_t nb;           // 64-column blocks per thread block (columns per block / 64)
 };
 
 struct TreeParams {
