@@ -528,6 +528,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--replays", type=int, default=200,
+                    help="identical-input replays per variant for the mismatch statistics")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -620,7 +622,7 @@ def main():
             split_sweep[str(S)] = {"us_per_layer": ms * 1e3 / W["layers"],
                                    "kernels_per_layer": ig.plan_query(sh)["apply_kernels"]}
             del g, wsS
-    replay = atomic_replay_stats(ig, st, 200)
+    replay = atomic_replay_stats(ig, st, max(2, args.replays))
 
     # dominant kernel roofline: per-launch CUDA-event durations
     kd = kernel_durations(ig, st, ws[ig.MODE_DET], max(20, args.steps // 4))
