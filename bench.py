@@ -193,10 +193,10 @@ class Stack:
         return n
 
 
-def make_shape(ig, st: Stack, mode, M=None, extra_flags=0):
+def make_shape(ig, st: Stack, mode, M=None, extra_flags=0, path=0):
     # inference weights are never written while the step runs
     return ig.make_shape(st.M if M is None else M, st.K, st.N, st.r, slices=st.slices,
-                         num_adapters=st.L, split_k=WORKLOAD["S"], mode=mode,
+                         num_adapters=st.L, split_k=WORKLOAD["S"], mode=mode, path=path,
                          flags=ig.FLAG_STATIC_WEIGHTS | extra_flags)
 
 
@@ -554,9 +554,15 @@ def main():
     for mode in (ig.MODE_DET, ig.MODE_ATOMIC, ig.MODE_UNSPLIT):
         ws[mode] = ig.workspace(make_shape(ig, st, mode), device=device)
     ws[ig.MODE_DET_TREE] = ig.workspace(make_shape(ig, st, ig.MODE_DET_TREE), device=device)
-    variants = (("det_sk8", ig.MODE_DET, 0), ("det_sk8_two_kernel", ig.MODE_DET, ig.FLAG_UNFUSED),
-                ("det_tree_sk8_two_launch", ig.MODE_DET_TREE, 0),
-                ("atomic_sk8", ig.MODE_ATOMIC, 0), ("unsplit_sk1", ig.MODE_UNSPLIT, 0))
+    # (name, mode, flags, path): the default (warp-level tensor-core) path in
+    # every mode, and the CUDA-core FMA path as its baseline
+    variants = (("det_sk8", ig.MODE_DET, 0, ig.PATH_AUTO),
+                ("det_sk8_two_kernel", ig.MODE_DET, ig.FLAG_UNFUSED, ig.PATH_AUTO),
+                ("det_tree_sk8_two_launch", ig.MODE_DET_TREE, 0, ig.PATH_AUTO),
+                ("atomic_sk8", ig.MODE_ATOMIC, 0, ig.PATH_AUTO),
+                ("unsplit_sk1", ig.MODE_UNSPLIT, 0, ig.PATH_AUTO),
+                ("det_sk8_cuda_core_fma", ig.MODE_DET, 0, ig.PATH_FMA),
+                ("atomic_sk8_cuda_core_fma", ig.MODE_ATOMIC, 0, ig.PATH_FMA))
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -565,8 +571,8 @@ def main():
     # main number: deterministic Split-K = 8
     results = {}
     graphs = {}
-    for name, mode, fl in variants:
-        sh = make_shape(ig, st, mode, extra_flags=fl)
+    for name, mode, fl, path in variants:
+        sh = make_shape(ig, st, mode, extra_flags=fl, path=path)
         g, launches = capture(ig, st, sh, ws[mode])
         graphs[name] = (g, launches)
         ms = time_graph(g, args.steps, max(3, args.warmup), world, device)
@@ -585,6 +591,8 @@ def main():
     det = results["det_sk8"]
     results["det_overhead_vs_atomic_pct"] = 100 * (det["ms_per_step"] /
                                                    results["atomic_sk8"]["ms_per_step"] - 1)
+    results["warp_mma_speedup_vs_cuda_core_fma_pct"] = 100 * (
+        results["det_sk8_cuda_core_fma"]["ms_per_step"] / det["ms_per_step"] - 1)
     results["det_two_kernel_overhead_vs_atomic_pct"] = 100 * (
         results["det_sk8_two_kernel"]["ms_per_step"] / results["atomic_sk8"]["ms_per_step"] - 1)
     results["det_speedup_vs_unsplit_pct"] = 100 * (results["unsplit_sk1"]["ms_per_step"] /
@@ -597,8 +605,8 @@ def main():
     if not args.no_sweep:
         for M in SWEEP_M:
             row = {}
-            for name, mode, fl in variants:
-                sh = make_shape(ig, st, mode, M=M, extra_flags=fl)
+            for name, mode, fl, path in variants:
+                sh = make_shape(ig, st, mode, M=M, extra_flags=fl, path=path)
                 g, _ = capture(ig, st, sh, ws[mode], M=M)
                 ms = time_graph(g, max(20, args.steps // 4), 3, world, device)
                 u = int(torch.unique(st.idx[:M]).numel())

@@ -102,8 +102,12 @@ typedef enum ig_path {
   IG_PATH_AUTO = 0,  /* chosen from (K, r, N, slices) only, never from M */
   IG_PATH_WARP = 1,  /* small ranks: 8-token tiles on the warp-level tensor
                         cores (bf16 mma.sync m16n8k16, FP32 accumulation) */
-  IG_PATH_MMA = 2    /* 128-token tiles on the tcgen05 tensor cores, FP32
+  IG_PATH_MMA = 2,   /* 128-token tiles on the tcgen05 tensor cores, FP32
                         accumulation in TMEM */
+  IG_PATH_FMA = 3    /* small ranks on CUDA cores: 8-token tiles, FP32 FMA in
+                        increasing k per lane, warp-shuffle butterfly across
+                        lanes; never chosen by IG_PATH_AUTO (the warp path
+                        measured faster), kept as the CUDA-core baseline */
 } ig_path;
 
 typedef struct ig_shape {
@@ -150,7 +154,7 @@ typedef struct ig_shape {
 /* The resolved plan. Everything that fixes the arithmetic is in
  * determinism_key, which never depends on M. */
 typedef struct ig_plan_info {
-  int32_t path;             /* IG_PATH_WARP or IG_PATH_MMA */
+  int32_t path;             /* IG_PATH_WARP, IG_PATH_MMA or IG_PATH_FMA */
   int32_t split_k;          /* S used (1 for IG_MODE_UNSPLIT) */
   int64_t k_split;          /* K / S: elements per partition */
   int32_t shrink_bm;        /* shrink output tile: token rows ... */
@@ -163,7 +167,7 @@ typedef struct ig_plan_info {
   uint64_t determinism_key; /* hash of the arithmetic-defining plan fields */
   int32_t apply_kernels;    /* kernels lora_apply launches after the token
                                map: 1 = fused shrink+expand (IG_MODE_DET,
-                               r = 8 or 16, S <= 16, warp path), 2 = shrink
+                               r = 8 or 16, S <= 16, warp or FMA path), 2 = shrink
                                then expand */
   int32_t reserved;
 } ig_plan_info;

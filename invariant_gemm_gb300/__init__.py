@@ -19,7 +19,7 @@ import ctypes
 import os
 
 __all__ = [
-    "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "MODE_DET_TREE", "PATH_AUTO", "PATH_WARP", "PATH_MMA",
+    "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "MODE_DET_TREE", "PATH_AUTO", "PATH_WARP", "PATH_MMA", "PATH_FMA",
     "FLAG_STATIC_WEIGHTS", "FLAG_UNFUSED", "FLAG_Z_FP32",
     "IGError", "Shape", "PlanInfo", "lib", "lib_path", "make_shape", "workspace_bytes",
     "plan_query", "workspace", "workspace_init", "map_tokens", "lora_shrink",
@@ -31,7 +31,7 @@ MODE_DET, MODE_ATOMIC, MODE_UNSPLIT, MODE_DET_TREE = 0, 1, 2, 3
 FLAG_STATIC_WEIGHTS = 1
 FLAG_UNFUSED = 2
 FLAG_Z_FP32 = 4
-PATH_AUTO, PATH_WARP, PATH_MMA = 0, 1, 2
+PATH_AUTO, PATH_WARP, PATH_MMA, PATH_FMA = 0, 1, 2, 3
 
 STATUS = {
     0: "IG_OK", -1: "IG_ERR_ARG", -2: "IG_ERR_SHAPE", -3: "IG_ERR_ALIGN",

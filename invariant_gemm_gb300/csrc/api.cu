@@ -41,7 +41,7 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   if ((sh->flags & ~(IG_FLAG_STATIC_WEIGHTS | IG_FLAG_UNFUSED | IG_FLAG_Z_FP32)) != 0)
     return IG_ERR_ARG;
   if (sh->mode < IG_MODE_DET || sh->mode > IG_MODE_DET_TREE) return IG_ERR_ARG;
-  if (sh->path < IG_PATH_AUTO || sh->path > IG_PATH_MMA) return IG_ERR_ARG;
+  if (sh->path < IG_PATH_AUTO || sh->path > IG_PATH_FMA) return IG_ERR_ARG;
   const int64_t M = sh->M, K = sh->K, N = sh->N, r = sh->r;
   if (M < 0 || K < 8 || N < 8 || r < 8) return IG_ERR_SHAPE;
   if (K % 8 || N % 8 || r % 8) return IG_ERR_SHAPE;
@@ -88,10 +88,11 @@ int make_plan(const ig_shape* sh, Plan* pl) {
 
   // The fused kernel expands N/S columns per block; past 1024 the two-kernel
   // path (256-column expand blocks) is faster. Both give the same bits.
-  pl->fused = sh->mode == IG_MODE_DET && path == IG_PATH_WARP && (r == 8 || r == 16) &&
-              pl->bn == r && S <= 16 && (N + S - 1) / S <= 1024 &&
-              !(sh->flags & IG_FLAG_UNFUSED) &&
-              fused_smem_bytes(pl->bn, pl->Ks, N, S) <= 200 * 1024;
+  const size_t fsmem = path == IG_PATH_FMA ? fused_fma_smem_bytes(pl->bn, pl->Ks, N, S)
+                                           : fused_smem_bytes(pl->bn, pl->Ks, N, S);
+  pl->fused = sh->mode == IG_MODE_DET && (path == IG_PATH_WARP || path == IG_PATH_FMA) &&
+              (r == 8 || r == 16) && pl->bn == r && S <= 16 && (N + S - 1) / S <= 1024 &&
+              !(sh->flags & IG_FLAG_UNFUSED) && fsmem <= 200 * 1024;
 
   uint64_t h = 1469598103934665603ull;
   const int64_t fields[] = {IG_ABI_VERSION, kArithRevision, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
@@ -247,14 +248,18 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   }
   if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st);
   ShrinkParams p;
+  const bool fma = pl.path == IG_PATH_FMA;
+  // warp path: 64-element boxes, 128-byte swizzle (ldmatrix operands);
+  // FMA path: 256-element k-blocks, no swizzle
+  const uint32_t kbox = fma ? kShrinkKB : 64;
+  const int swz = fma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+                         kbox, 1, swz);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
-                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)pl.bn,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)pl.bn, swz);
   if (rc != IG_OK) return rc;
-  p.has_a3 = sh->K % 64 == 0 && pl.Ks % 64 == 0;
+  p.has_a3 = !fma && sh->K % 64 == 0 && pl.Ks % 64 == 0;
   if (p.has_a3) {
     rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                        (uint64_t)sh->K, (uint32_t)pl.bn);
@@ -277,21 +282,24 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   p.jblocks = pl.jblocks;
   p.flags = sh->flags;
   p.scale = scale;
+  if (fma) return cuda_status(launch_shrink_fma(p, pl.mode, pl.bn, pl.tiles, st));
   return cuda_status(launch_shrink_warp(p, pl.mode, pl.bn, pl.tiles, st));
 }
 
 int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, const void* B,
               float scale, float* z, void* y, uint8_t* ws, cudaStream_t st) {
   FusedParams p;
-  // x rows are gathered 4 at a time (box 64 x 1); A blocks are r rows high
+  const bool fma = pl.path == IG_PATH_FMA;
+  // x rows are gathered 4 at a time (box kbox x 1); A blocks are r rows high
+  const uint32_t kbox = fma ? kShrinkKB : 64;
+  const int swz = fma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+                         kbox, 1, swz);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
-                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)sh->r,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)sh->r, swz);
   if (rc != IG_OK) return rc;
-  p.has_a3 = sh->K % 64 == 0 && pl.Ks % 64 == 0;
+  p.has_a3 = !fma && sh->K % 64 == 0 && pl.Ks % 64 == 0;
   if (p.has_a3) {
     rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                        (uint64_t)sh->K, (uint32_t)sh->r);
@@ -299,7 +307,8 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
   }
   // B as rows of 64 elements (64 / r output columns x r ranks), 128-byte
   // swizzled boxes of b_box_rows rows
-  p.b_box_rows = fused_b_box_rows(pl.bn, pl.Ks, sh->N, pl.S);
+  p.b_box_rows = fma ? fused_fma_b_box_rows(pl.bn, pl.Ks, sh->N, pl.S)
+                     : fused_b_box_rows(pl.bn, pl.Ks, sh->N, pl.S);
   rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N * sh->r / 64,
                      64, 128, 64, (uint32_t)p.b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
@@ -319,6 +328,7 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
   p.S = pl.S;
   p.flags = sh->flags;
   p.scale = scale;
+  if (fma) return cuda_status(launch_fused_fma(p, pl.bn, pl.tiles, st));
   return cuda_status(launch_fused_warp(p, pl.bn, pl.tiles, st));
 }
 
@@ -326,10 +336,13 @@ int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B
                uint8_t* ws, cudaStream_t st) {
   if (pl.path == IG_PATH_MMA) return run_expand_mma(sh, pl, z, B, y, ws, st);
   ExpandParams p;
-  int rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N * sh->r / 64,
-                         64, 128, 64, (uint32_t)expand_warp_box_rows((int)sh->r, sh->N),
-                         CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc != IG_OK) return rc;
+  if (pl.path != IG_PATH_FMA) {   // the FMA expand copies B with 1-D bulk copies
+    int rc = encode_map_2d(&p.tm_b, B,
+                           (uint64_t)sh->num_adapters * sh->slices * sh->N * sh->r / 64, 64, 128,
+                           64, (uint32_t)expand_warp_box_rows((int)sh->r, sh->N),
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != IG_OK) return rc;
+  }
   p.z = z;
   p.B = static_cast<const __nv_bfloat16*>(B);
   p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
@@ -342,6 +355,7 @@ int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B
   p.L = sh->num_adapters;
   p.ntiles = pl.ntiles;
   p.flags = sh->flags;
+  if (pl.path == IG_PATH_FMA) return cuda_status(launch_expand_fma(p, pl.tiles, st));
   return cuda_status(launch_expand_warp(p, pl.tiles, st));
 }
 

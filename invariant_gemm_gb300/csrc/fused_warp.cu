@@ -39,9 +39,6 @@ namespace ig {
 
 namespace {
 
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
-}
 
 template <int BN>
 struct FusedGeo {

@@ -184,6 +184,13 @@ cudaError_t launch_fused_warp(const FusedParams& p, int bn, int64_t tiles_max, c
 size_t fused_smem_bytes(int bn, int64_t Ks, int64_t N, int S);
 int fused_b_box_rows(int bn, int64_t Ks, int64_t N, int S);
 size_t expand_warp_smem_bytes(int r, int64_t N);
+// IG_PATH_FMA (CUDA cores): the same kernel roles with FP32 FMA arithmetic
+cudaError_t launch_shrink_fma(const ShrinkParams& p, int mode, int bn, int64_t tiles_max,
+                              cudaStream_t st);
+cudaError_t launch_expand_fma(const ExpandParams& p, int64_t tiles_max, cudaStream_t st);
+cudaError_t launch_fused_fma(const FusedParams& p, int bn, int64_t tiles_max, cudaStream_t st);
+size_t fused_fma_smem_bytes(int bn, int64_t Ks, int64_t N, int S);
+int fused_fma_b_box_rows(int bn, int64_t Ks, int64_t N, int S);
 int expand_warp_box_rows(int r, int64_t N);
 cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
                               cudaStream_t st);
@@ -327,6 +334,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote, float4 v, uint32_t 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Fetch a kernel-parameter tensor map into the descriptor cache early.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
 // Tiled 2-D tensor copy global -> shared (box of the tensor map at

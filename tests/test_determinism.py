@@ -300,19 +300,21 @@ FUSED_CASES = [
 ]
 
 
+@pytest.mark.parametrize("path", [ig.PATH_WARP, ig.PATH_FMA], ids=["warp", "fma"])
 @pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "M%d_K%d_N%d_r%d_sl%d_S%d" % (
     c[0], c[1], c[2], c[3], c[4], c[6]))
-def test_fused_apply_bitwise_equals_two_kernels(case):
+def test_fused_apply_bitwise_equals_two_kernels(case, path):
     """lora_apply's one-launch cluster kernel (DET) and the two-kernel path
     (Split-K shrink with the counter protocol, then expand) give the same bits
-    for z and y; and both are within tolerance of the oracle."""
+    for z and y, on the warp-level tensor-core path and on the CUDA-core FMA
+    path; and both are within tolerance of the oracle."""
     M, K, N, r, slices, L, S, none_frac = case
     p = synth.make_problem(M, K, N, r, slices=slices, L=L, seed=M + K + S,
                            none_frac=none_frac, device="cuda")
     outs = []
     for flags in (0, ig.FLAG_UNFUSED, ig.FLAG_STATIC_WEIGHTS):
         sh = ig.make_shape(M, K, N, r, slices=slices, num_adapters=L, split_k=S,
-                           mode=ig.MODE_DET, flags=flags)
+                           mode=ig.MODE_DET, path=path, flags=flags)
         if flags != ig.FLAG_UNFUSED:
             assert ig.plan_query(sh)["apply_kernels"] == 1
         z, y = run_apply(p, mode=ig.MODE_DET, split_k=S, ws=ig.workspace(sh),
@@ -325,19 +327,20 @@ def test_fused_apply_bitwise_equals_two_kernels(case):
     check_expand(p.to("cpu"), outs[0][0], outs[0][1])
 
 
+@pytest.mark.parametrize("path", [ig.PATH_WARP, ig.PATH_FMA], ids=["warp", "fma"])
 @pytest.mark.parametrize("flags", [0, ig.FLAG_UNFUSED], ids=["fused", "two_kernel"])
-def test_batch_invariance_rank16(flags):
+def test_batch_invariance_rank16(flags, path):
     """Batch invariance of 64 probe rows at r = 16 (the fused kernel's rank)
-    over batch sizes 1..512."""
+    over batch sizes 1..512, on both small-rank paths."""
     K, N, r, L = 4096, 1024, 16, 8
     base = synth.make_problem(64, K, N, r, L=L, seed=2003, device="cuda")
-    sh0 = ig.make_shape(512, K, N, r, num_adapters=L, split_k=8, flags=flags)
+    sh0 = ig.make_shape(512, K, N, r, num_adapters=L, split_k=8, path=path, flags=flags)
     ws = ig.workspace(sh0)
     ref_z = ref_y = None
     for b in range(1, 513):
         x, y, idx, pos = synth.probe_batch(base.x, base.y, base.idx, b, L, seed=9000 + b,
                                            device="cuda")
-        sh = ig.make_shape(b, K, N, r, num_adapters=L, split_k=8, flags=flags)
+        sh = ig.make_shape(b, K, N, r, num_adapters=L, split_k=8, path=path, flags=flags)
         z = torch.empty((1, b, r), dtype=torch.float32, device="cuda")
         ig.lora_apply(sh, x, y, idx, base.A, base.B, base.scale, z, ws)
         pz = z[0, pos].view(torch.int32)

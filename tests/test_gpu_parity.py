@@ -145,3 +145,34 @@ def test_max_adapters_and_all_none():
     z, y = run_apply(p)
     assert torch.all(z == 0)
     assert torch.equal(y, p.y)
+
+
+@pytest.mark.parametrize("mode", MODES + [ig.MODE_DET_TREE], ids=lambda m: MODE_ID.get(m, "tree"))
+@pytest.mark.parametrize("r", [8, 16, 24])
+def test_fma_path_parity(r, mode):
+    """IG_PATH_FMA (CUDA-core FP32 FMA, warp-shuffle reduction): every mode,
+    against the oracle; small integers bit-exact."""
+    p = synth.make_problem(150, 11008, 264, r, slices=2, L=5, seed=400 + r, none_frac=0.2,
+                           device="cuda")
+    z, y = run_apply(p, mode=mode, path=ig.PATH_FMA)
+    check_shrink(p.to("cpu"), z)
+    check_expand(p.to("cpu"), z, y)
+    pi = synth.make_problem(40, 4096, 512, r, L=3, seed=500 + r, dist="int", device="cuda")
+    z, y = run_apply(pi, mode=mode, path=ig.PATH_FMA)
+    check_shrink(pi.to("cpu"), z, exact=True)
+    check_expand(pi.to("cpu"), z, y, exact=True)
+
+
+def test_fma_and_warp_paths_differ_only_within_tolerance():
+    """The two small-rank paths sum each partition in a different order
+    (FMA chains and a butterfly against tensor-core MMAs); the plan keeps
+    them apart in the determinism key, and both meet the oracle's bound."""
+    p = synth.make_problem(64, 4096, 1024, 16, L=4, seed=77, device="cuda")
+    keys = []
+    for path in (ig.PATH_WARP, ig.PATH_FMA):
+        sh = ig.make_shape(p.M, p.K, p.N, 16, num_adapters=4, path=path)
+        keys.append(ig.plan_query(sh)["determinism_key"])
+        z, y = run_apply(p, shape=sh)
+        check_shrink(p.to("cpu"), z)
+        check_expand(p.to("cpu"), z, y)
+    assert keys[0] != keys[1]
