@@ -249,12 +249,12 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st);
   ShrinkParams p;
   const bool fma = pl.path == IG_PATH_FMA;
-  // warp path: 64-element boxes, 128-byte swizzle (ldmatrix operands);
-  // FMA path: 256-element k-blocks, no swizzle
+  // x: 256-element rows, no swizzle (both paths); A: warp path 64-element
+  // boxes, 128-byte swizzle (ldmatrix operands), FMA path 256, no swizzle
   const uint32_t kbox = fma ? kShrinkKB : 64;
   const int swz = fma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         kbox, 1, swz);
+                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)pl.bn, swz);
@@ -290,11 +290,11 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
               float scale, float* z, void* y, uint8_t* ws, cudaStream_t st) {
   FusedParams p;
   const bool fma = pl.path == IG_PATH_FMA;
-  // x rows are gathered 4 at a time (box kbox x 1); A blocks are r rows high
+  // x rows are gathered 4 at a time (box 256 x 1); A blocks are r rows high
   const uint32_t kbox = fma ? kShrinkKB : 64;
   const int swz = fma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         kbox, 1, swz);
+                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)sh->r, swz);

@@ -79,7 +79,7 @@ struct MapParams {
 };
 
 struct ShrinkParams {
-  CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (row gathers)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x BN, 128-byte swizzle
   CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, BN, 4} (when has_a3)
   const __nv_bfloat16* x;
@@ -119,7 +119,7 @@ int encode_map_a3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
                   uint32_t box_rows);
 
 struct FusedParams {
-  CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
+  CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (row gathers)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
   CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, r, 4} (when has_a3)
   CUtensorMap tm_b;     // B_stack as rows of 64 elements (64/r output columns

@@ -5,12 +5,16 @@
 // Tile: up to 8 token rows x BN rank columns (BN = 8 or 16); the block has
 // BN/4 warps (4 or 2) and ends with one output per thread: thread o holds
 // the partial of token row o / BN, rank o % BN. The partition [k0, k0 + Ks)
-// is streamed through a ring of `nst` shared-memory stages of 256 elements,
-// each stage four 64-element sub-blocks written by TMA copies with 128-byte
-// swizzle (the BN A rows of all four sub-blocks by one 3-D tiled copy when
-// K and K/S are multiples of 64, else one 2-D copy per sub-block; one row
-// gather per 4 token rows per sub-block; completion counted in bytes on one
-// mbarrier per stage); warp 0 issues the copies.
+// is streamed through a ring of `nst` shared-memory stages of 256 elements:
+// the BN A rows as four 64-element sub-blocks, 128-byte swizzled (one 3-D
+// TMA copy when K and K/S are multiples of 64, else one 2-D copy per
+// sub-block), and the token rows of x unswizzled, 512 bytes each (one row
+// gather per 4 tokens; a last group of one token by a tiled copy); completion
+// is counted in bytes on one mbarrier per stage, and warp 0 issues the copies.
+// The x operand rows of the MMA past nrows read the tile's last row (the same
+// address: a broadcast); a full tile's 8 rows share banks (8-way ldmatrix
+// conflicts on x), which measured cheaper than the four swizzled 64-element
+// copies per k-block a conflict-free layout needs.
 //
 // Order of the sum, identical for every row and every M ("Reproducible LoRA
 // Inference Through Deterministic Split-K Reduction" leaves the order inside
@@ -40,7 +44,7 @@ struct PartialArgs {
   uint32_t* status;
   int64_t Ks;                 // partition length
   int nrows;
-  const CUtensorMap* tm_x;    // x [M][K], box 64 x 1, 128-byte swizzle
+  const CUtensorMap* tm_x;    // x [M][K], box 256 x 1, no swizzle
   const CUtensorMap* tm_a;    // A as [rows][K], box 64 x BN, 128-byte swizzle
   const CUtensorMap* tm_a3;   // A as {64, rows, K/64}, box {64, BN, 4}, or null
   int k0;                     // partition start (column coordinate)
@@ -51,9 +55,10 @@ template <int BN>
 struct PartialRing {
   using G = ShrinkGeo<BN>;
   static constexpr int kSub = kShrinkKB / 64;                 // 64-element sub-blocks
-  static constexpr int kXBytes = kSub * kTileRows * 128;      // [sub][8 rows][128 B]
+  static constexpr int kXBytes = kTileRows * kShrinkKB * 2;   // [8 rows][512 B]
   static constexpr int kABytes = kSub * BN * 128;             // [sub][BN rows][128 B]
   static constexpr int kStageBytes = kXBytes + kABytes;       // multiple of 1024
+  static constexpr int kRowBytes = kShrinkKB * 2;             // x row (512 B)
   uint8_t* stages;   // 1024-aligned
   uint64_t* bars;
   int nst;      // ring depth
@@ -65,14 +70,15 @@ struct PartialRing {
   __device__ __forceinline__ int nsub(const PartialArgs& a, int b) const {
     return (klen(a, b) + 63) / 64;
   }
-  // x rows copied per sub-block: 4 per row gather; a last group holding one
-  // row is copied by a one-row tiled load instead (no repeated rows)
+  // x rows copied: 4 per row gather; a last group holding one row is copied
+  // by a one-row tiled load instead (no repeated rows)
   __device__ __forceinline__ static int x_rows_copied(int nrows) {
     return (nrows / 4) * 4 + (nrows % 4 == 1 ? 1 : (nrows % 4 ? 4 : 0));
   }
   // warp 0: arm stage b % nst for all copies of k-block b
   __device__ __forceinline__ void expect(const PartialArgs& a, int b) const {
-    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * (BN + x_rows_copied(a.nrows));
+    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * BN +
+                           (uint32_t)kRowBytes * x_rows_copied(a.nrows);
     if ((threadIdx.x & 31) == 0) mbar_arrive_expect_tx(&bars[b % nst], bytes);
     __syncwarp();
   }
@@ -94,18 +100,16 @@ struct PartialRing {
     uint8_t* sx = stages + st * kStageBytes;
     const int groups4 = (a.nrows + 3) / 4;
     const int last = a.nrows - 1;
-    // one lane per (sub-block, group of 4 rows); in a group of 2 or 3 rows
-    // the last row repeats (loaded, never used); a group of one row is one
-    // tiled copy of that row
-    if (lane < nsub(a, b) * groups4) {
-      const int q = lane / groups4, gq = lane % groups4;
-      uint8_t* dst = sx + q * 1024 + gq * 512;
-      const int kc = a.k0 + b * kShrinkKB + q * 64;
-      if (4 * gq == last)
+    // one lane per group of 4 rows; in a group of 2 or 3 rows the last row
+    // repeats (loaded, never used); a group of one row is one tiled copy
+    if (lane < groups4) {
+      uint8_t* dst = sx + lane * 4 * kRowBytes;
+      const int kc = a.k0 + b * kShrinkKB;
+      if (4 * lane == last)
         tma_load_2d(dst, a.tm_x, kc, a.rows[last], &bars[st]);
       else
-        tma_gather4(dst, a.tm_x, kc, a.rows[4 * gq], a.rows[min(4 * gq + 1, last)],
-                    a.rows[min(4 * gq + 2, last)], a.rows[min(4 * gq + 3, last)], &bars[st]);
+        tma_gather4(dst, a.tm_x, kc, a.rows[4 * lane], a.rows[min(4 * lane + 1, last)],
+                    a.rows[min(4 * lane + 2, last)], a.rows[min(4 * lane + 3, last)], &bars[st]);
     }
   }
 
@@ -119,7 +123,7 @@ struct PartialRing {
     // ldmatrix row addresses of this lane: A (ranks) rows and x (tokens) rows
     const int arow = (lane & 7) + (BN == 16 ? 8 * ((lane >> 3) & 1) : 0);
     const int achunk = BN == 16 ? (lane >> 4) : ((lane >> 3) & 1);
-    const int xrow = lane & 7;
+    const int xrow = min(lane & 7, a.nrows - 1);   // this lane's token row
     const int xchunk = (lane >> 3) & 1;
 
     int issued = min(nkb, nst);
@@ -144,7 +148,7 @@ struct PartialRing {
                   af[0], af[2]);
           af[1] = af[3] = 0u;
         }
-        ldsm_x2(sx + q * 1024 + xrow * 128 + (((c16 + xchunk) ^ xrow) << 4), bf[0], bf[1]);
+        ldsm_x2(sx + xrow * kRowBytes + kk * 32 + xchunk * 16, bf[0], bf[1]);
       };
       if (kl == kShrinkKB) {
         // full k-block: this warp's 16 / W steps, all operands first, then the
@@ -173,7 +177,7 @@ struct PartialRing {
           ldsm_x1(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0);
           a1 = 0u;
         }
-        ldsm_x1(sx + q * 1024 + xrow * 128 + ((c ^ xrow) << 4), b0);
+        ldsm_x1(sx + xrow * kRowBytes + n16 * 32, b0);
         mma_1688(d, a0, a1, b0);
       }
       __syncthreads();
