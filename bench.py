@@ -246,12 +246,13 @@ def time_graph(g, steps, warmup, world, device):
 
 def kernel_durations(ig, st, ws, steps):
     """Average device duration per launch of each kernel of the step: the
-    fused shrink+expand kernel (lora_apply, DET), and the two-kernel path's
-    Split-K shrink (counter protocol) and expand. Each is captured as
+    fused shrink+expand kernel (lora_apply, DET), and lora_shrink and
+    lora_expand called separately (the Split-K shrink with its cluster
+    combine, and the expand). Each is captured as
     `layers` back-to-back launches (token map built once beforehand) in its
     own CUDA graph and timed with CUDA events on the launching stream."""
     fused = make_shape(ig, st, ig.MODE_DET)
-    two = make_shape(ig, st, ig.MODE_DET, extra_flags=ig.FLAG_UNFUSED)
+    two = fused    # lora_shrink / lora_expand called separately, default plan
     ig.map_tokens(fused, st.idx, ws)
     torch.cuda.synchronize()
 
@@ -636,10 +637,10 @@ def main():
     kd = kernel_durations(ig, st, ws[ig.MODE_DET], max(20, args.steps // 4))
     b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
     kern = {"fused_warp (lora_apply, det)": (kd["fused"], b["total"], "fused_warp.cu"),
-            "shrink_warp (lora_shrink, det, two-kernel path)": (kd["shrink"], b["shrink"],
-                                                               "shrink_warp.cu"),
-            "expand_warp (lora_expand, two-kernel path)": (kd["expand"], b["expand"],
-                                                          "expand_warp.cu")}
+            "shrink_warp (lora_shrink alone, det, cluster combine)": (kd["shrink"],
+                                                                      b["shrink"],
+                                                                      "shrink_warp.cu"),
+            "expand_warp (lora_expand alone)": (kd["expand"], b["expand"], "expand_warp.cu")}
     dom = "fused_warp (lora_apply, det)"
     d_ms, d_bytes, d_file = kern[dom]
     achieved = d_bytes / (d_ms * 1e-3) / 1e9

@@ -256,10 +256,16 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
                          kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != IG_OK) return rc;
+  if (!fma) {
+    rc = encode_map_2d(&p.tm_xs, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
+                       1, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != IG_OK) return rc;
+  }
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)pl.bn, swz);
   if (rc != IG_OK) return rc;
   p.has_a3 = !fma && sh->K % 64 == 0 && pl.Ks % 64 == 0;
+  p.x_wide_rows = sh->M >= kXWideMinM ? kTileRows : kTileRows + 1;
   if (p.has_a3) {
     rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                        (uint64_t)sh->K, (uint32_t)pl.bn);
@@ -296,10 +302,16 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
                          kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != IG_OK) return rc;
+  if (!fma) {
+    rc = encode_map_2d(&p.tm_xs, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
+                       1, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != IG_OK) return rc;
+  }
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)sh->r, swz);
   if (rc != IG_OK) return rc;
   p.has_a3 = !fma && sh->K % 64 == 0 && pl.Ks % 64 == 0;
+  p.x_wide_rows = sh->M >= kXWideMinM ? kTileRows : kTileRows + 1;
   if (p.has_a3) {
     rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                        (uint64_t)sh->K, (uint32_t)sh->r);

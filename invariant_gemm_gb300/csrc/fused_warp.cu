@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   pa.Ks = p.Ks;
   pa.nrows = nrows;
   pa.tm_x = &p.tm_x;
+  pa.tm_xs = &p.tm_xs;
+  pa.wide_rows = p.x_wide_rows;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)((int64_t)s * p.Ks);

@@ -50,6 +50,9 @@ constexpr int kShrinkKB = 256;        // elements per k-block (4 swizzled sub-bl
 constexpr int kShrinkStages = 4;
 constexpr int kExpandWarps = 4;
 constexpr int kExpandBN = 256;        // output columns per expand block: 4 warps x 8 blocks of 8
+// Small-rank path: full tiles take x swizzled from this batch size on (a
+// copy layout only: results do not depend on it).
+constexpr int64_t kXWideMinM = 128;
 // Revision of the arithmetic of the kernels; part of the determinism key.
 constexpr int kArithRevision = 2;
 // tensor-core path: 128-row tiles (the MMA's M)
@@ -80,6 +83,7 @@ struct MapParams {
 
 struct ShrinkParams {
   CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (row gathers)
+  CUtensorMap tm_xs;    // x [M][K], box 64 x 1, 128-byte swizzle (full tiles)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x BN, 128-byte swizzle
   CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, BN, 4} (when has_a3)
   const __nv_bfloat16* x;
@@ -92,6 +96,7 @@ struct ShrinkParams {
   int64_t M, K, r, Ks;
   int32_t slices, L, S, jblocks, flags;
   int32_t has_a3;       // K and K/S multiples of 64: one 3-D copy per k-block of A
+  int32_t x_wide_rows;  // tiles of this many tokens or more take x swizzled
   float scale;
 };
 
@@ -120,6 +125,7 @@ int encode_map_a3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
 
 struct FusedParams {
   CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (row gathers)
+  CUtensorMap tm_xs;    // x [M][K], box 64 x 1, 128-byte swizzle (full tiles)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
   CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, r, 4} (when has_a3)
   CUtensorMap tm_b;     // B_stack as rows of 64 elements (64/r output columns
@@ -135,6 +141,7 @@ struct FusedParams {
   int32_t slices, L, S, flags;
   int32_t b_box_rows;
   int32_t has_a3;
+  int32_t x_wide_rows;  // tiles of this many tokens or more take x swizzled
   float scale;
 };
 

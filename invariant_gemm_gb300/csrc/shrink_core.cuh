@@ -12,9 +12,10 @@
 // gather per 4 tokens; a last group of one token by a tiled copy); completion
 // is counted in bytes on one mbarrier per stage, and warp 0 issues the copies.
 // The x operand rows of the MMA past nrows read the tile's last row (the same
-// address: a broadcast); a full tile's 8 rows share banks (8-way ldmatrix
-// conflicts on x), which measured cheaper than the four swizzled 64-element
-// copies per k-block a conflict-free layout needs.
+// address: a broadcast). Full tiles of large batches take x swizzled instead
+// (64-element sub-blocks: conflict-free ldmatrix, four copies per k-block);
+// at small batches the one-copy layout's shorter latency wins. Either way the
+// operand values, and so the results, are the same.
 //
 // Order of the sum, identical for every row and every M ("Reproducible LoRA
 // Inference Through Deterministic Split-K Reduction" leaves the order inside
@@ -45,10 +46,12 @@ struct PartialArgs {
   int64_t Ks;                 // partition length
   int nrows;
   const CUtensorMap* tm_x;    // x [M][K], box 256 x 1, no swizzle
+  const CUtensorMap* tm_xs;   // x [M][K], box 64 x 1, 128-byte swizzle (wide tiles)
   const CUtensorMap* tm_a;    // A as [rows][K], box 64 x BN, 128-byte swizzle
   const CUtensorMap* tm_a3;   // A as {64, rows, K/64}, box {64, BN, 4}, or null
   int k0;                     // partition start (column coordinate)
   int a_row;                  // row coordinate of the tile's first A row
+  int wide_rows;              // tiles of this many tokens or more: swizzled x
 };
 
 template <int BN>
@@ -75,10 +78,19 @@ struct PartialRing {
   __device__ __forceinline__ static int x_rows_copied(int nrows) {
     return (nrows / 4) * 4 + (nrows % 4 == 1 ? 1 : (nrows % 4 ? 4 : 0));
   }
+  // Tiles of at least a.wide_rows tokens take x in 64-element,
+  // 128-byte-swizzled sub-blocks (conflict-free ldmatrix, four copies per
+  // k-block); smaller tiles take unswizzled 512-byte rows (one copy per
+  // k-block). Same operand values, same results: the host picks the
+  // threshold from the batch size.
+  __device__ __forceinline__ static bool wide(const PartialArgs& a) {
+    return a.nrows >= a.wide_rows;
+  }
   // warp 0: arm stage b % nst for all copies of k-block b
   __device__ __forceinline__ void expect(const PartialArgs& a, int b) const {
-    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * BN +
-                           (uint32_t)kRowBytes * x_rows_copied(a.nrows);
+    const uint32_t xb = wide(a) ? (uint32_t)nsub(a, b) * 128u * x_rows_copied(a.nrows)
+                                : (uint32_t)kRowBytes * x_rows_copied(a.nrows);
+    const uint32_t bytes = (uint32_t)nsub(a, b) * 128u * BN + xb;
     if ((threadIdx.x & 31) == 0) mbar_arrive_expect_tx(&bars[b % nst], bytes);
     __syncwarp();
   }
@@ -100,6 +112,20 @@ struct PartialRing {
     uint8_t* sx = stages + st * kStageBytes;
     const int groups4 = (a.nrows + 3) / 4;
     const int last = a.nrows - 1;
+    if (wide(a)) {
+      // one lane per (sub-block, group of 4 rows), 128-byte swizzled
+      if (lane < nsub(a, b) * groups4) {
+        const int q = lane / groups4, gq = lane % groups4;
+        uint8_t* dst = sx + q * 1024 + gq * 512;
+        const int kc = a.k0 + b * kShrinkKB + q * 64;
+        if (4 * gq == last)
+          tma_load_2d(dst, a.tm_xs, kc, a.rows[last], &bars[st]);
+        else
+          tma_gather4(dst, a.tm_xs, kc, a.rows[4 * gq], a.rows[min(4 * gq + 1, last)],
+                      a.rows[min(4 * gq + 2, last)], a.rows[min(4 * gq + 3, last)], &bars[st]);
+      }
+      return;
+    }
     // one lane per group of 4 rows; in a group of 2 or 3 rows the last row
     // repeats (loaded, never used); a group of one row is one tiled copy
     if (lane < groups4) {
@@ -125,6 +151,7 @@ struct PartialRing {
     const int achunk = BN == 16 ? (lane >> 4) : ((lane >> 3) & 1);
     const int xrow = min(lane & 7, a.nrows - 1);   // this lane's token row
     const int xchunk = (lane >> 3) & 1;
+    const bool wd = wide(a);
 
     int issued = min(nkb, nst);
     int fail_b = -1;
@@ -148,7 +175,10 @@ struct PartialRing {
                   af[0], af[2]);
           af[1] = af[3] = 0u;
         }
-        ldsm_x2(sx + xrow * kRowBytes + kk * 32 + xchunk * 16, bf[0], bf[1]);
+        if (wd)
+          ldsm_x2(sx + q * 1024 + xrow * 128 + (((c16 + xchunk) ^ xrow) << 4), bf[0], bf[1]);
+        else
+          ldsm_x2(sx + xrow * kRowBytes + kk * 32 + xchunk * 16, bf[0], bf[1]);
       };
       if (kl == kShrinkKB) {
         // full k-block: this warp's 16 / W steps, all operands first, then the
@@ -177,7 +207,10 @@ struct PartialRing {
           ldsm_x1(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0);
           a1 = 0u;
         }
-        ldsm_x1(sx + xrow * kRowBytes + n16 * 32, b0);
+        if (wd)
+          ldsm_x1(sx + q * 1024 + xrow * 128 + ((c ^ xrow) << 4), b0);
+        else
+          ldsm_x1(sx + xrow * kRowBytes + n16 * 32, b0);
         mma_1688(d, a0, a1, b0);
       }
       __syncthreads();

@@ -28,6 +28,9 @@
 // dealt round-robin to the warps, each warp's steps accumulated in increasing
 // k by bf16 MMAs into FP32, then the warp sums added in warp order. It
 // depends only on K/S and BN.
+#include <map>
+#include <mutex>
+
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -41,7 +44,12 @@ struct ShrinkSmem {
   static constexpr int kBytes = 1024 + kStagesOff + kShrinkStages * PartialRing<BN>::kStageBytes;
 };
 
-template <int BN, int MODE>
+// CL (IG_MODE_DET only): the S partition blocks of a tile form a cluster;
+// block s owns outputs [s TB/S, (s+1) TB/S) of the tile and receives their S
+// partials by asynchronous remote stores counted on its mbarrier, then sums
+// them from FP32 zero in increasing partition order (the counter protocol's
+// order, so the same bits) without the workspace round trip.
+template <int BN, int MODE, bool CL>
 __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     shrink_warp_kernel(const __grid_constant__ ShrinkParams p) {
   using SM = ShrinkSmem<BN>;
@@ -50,8 +58,11 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* bar_recv = bars + kShrinkStages;                 // cluster combine
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);    // tile entry (kTileInts)
   int32_t* info = reinterpret_cast<int32_t*>(smem + 192);
+  float* recv = reinterpret_cast<float*>(smem + 256);        // [S][TB/S] (TB floats)
+  constexpr int TB = ShrinkGeo<BN>::TB;
   uint8_t* stages = smem + SM::kStagesOff;
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -69,7 +80,9 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
   if (tid == 0) {
     for (int i = 0; i < kShrinkStages; ++i) mbar_init(&bars[i], 1);
+    if (CL) mbar_init(bar_recv, 1);
     fence_mbar_init();
+    if (CL) mbar_arrive_expect_tx(bar_recv, (uint32_t)(TB * 4));
   }
   __syncthreads();
   const int g = ent_s[0];
@@ -92,6 +105,9 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     return;
   }
 
+  // every block of the cluster has initialised and armed its mbarrier once
+  // the matching cluster_wait returns
+  if (CL) cluster_arrive_relaxed();
   const int64_t k0 = (int64_t)s * p.Ks;
   const bool early_a = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
   PartialArgs pa;
@@ -100,6 +116,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   pa.Ks = p.Ks;
   pa.nrows = nrows;
   pa.tm_x = &p.tm_x;
+  pa.tm_xs = &p.tm_xs;
+  pa.wide_rows = p.x_wide_rows;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)k0;
@@ -127,7 +145,30 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   }
 
   float v;
-  if (!ring.run(pa, v)) return;
+  const bool ok = ring.run(pa, v);
+  if (CL) {
+    // Send output tid's partial to its owner; every block sends on every
+    // path (zeros after a failed copy), so every owner receives TB * 4 bytes.
+    const int per = TB / S;
+    cluster_wait();
+    const int owner = tid / per;
+    st_async_f32(map_rank(recv + s * per + tid % per, (uint32_t)owner), ok ? v : 0.0f,
+                 map_rank(bar_recv, (uint32_t)owner));
+    // The wait outlasts any sender's bounded waits, so the block never leaves
+    // while a partial is still on its way to it.
+    const bool got = mbar_wait_bounded(bar_recv, 0, p.status, 1ll << 36);
+    if (got && tid < per) {
+      const int o = s * per + tid;
+      const int row = o / BN, j = o % BN;
+      if (row < nrows) {
+        float total = 0.0f;
+        for (int q = 0; q < S; ++q) total += recv[q * per + tid];
+        p.z[((int64_t)sl * M + rows_s[row]) * r + jb * BN + j] = total * p.scale;
+      }
+    }
+    return;
+  }
+  if (!ok) return;
   const int rrow = tid / BN;                 // this thread's output
   const int j0 = tid % BN;
 
@@ -170,7 +211,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
 template <int BN, int MODE>
 cudaError_t launch_one(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
   using SM = ShrinkSmem<BN>;
-  auto kern = shrink_warp_kernel<BN, MODE>;
+  auto kern = shrink_warp_kernel<BN, MODE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SM::kBytes);
   if (e != cudaSuccess) return e;
@@ -180,18 +221,81 @@ cudaError_t launch_one(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st
   return launch_pdl(kern, dim3((unsigned)grid), dim3(ShrinkGeo<BN>::THREADS), SM::kBytes, st, p);
 }
 
+// Deterministic combine inside a cluster of the S partition blocks (same
+// bits as the counter protocol). Returns cudaErrorNotSupported when such a
+// cluster cannot be resident, for the caller to use the counter protocol.
+template <int BN>
+cudaError_t launch_cluster(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
+  using SM = ShrinkSmem<BN>;
+  auto kern = shrink_warp_kernel<BN, IG_MODE_DET, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SM::kBytes);
+  if (e != cudaSuccess) return e;
+  if (p.S > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t grid = tiles_max * p.slices * p.jblocks * p.S;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(ShrinkGeo<BN>::THREADS);
+  cfg.dynamicSmemBytes = SM::kBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  {
+    // can one such cluster be resident? (cached per S)
+    static std::mutex mu;
+    static std::map<int, bool> fits;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = fits.find(p.S);
+    if (it == fits.end()) {
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3((unsigned)p.S);
+      int n = 0;
+      const bool ok = cudaOccupancyMaxActiveClusters(&n, kern, &q) == cudaSuccess && n >= 1;
+      cudaGetLastError();
+      it = fits.emplace(p.S, ok).first;
+    }
+    if (!it->second) return cudaErrorNotSupported;
+  }
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_det(const ShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
+  constexpr int TB = ShrinkGeo<BN>::TB;
+  if (!(p.flags & IG_FLAG_UNFUSED) && p.S <= 16 && TB % p.S == 0) {
+    const cudaError_t e = launch_cluster<BN>(p, tiles_max, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  return launch_one<BN, IG_MODE_DET>(p, tiles_max, st);
+}
+
 }  // namespace
 
 cudaError_t launch_shrink_warp(const ShrinkParams& p, int mode, int bn, int64_t tiles_max,
                               cudaStream_t st) {
   if (bn == 16) {
     if (mode == IG_MODE_DET_TREE) return launch_one<16, IG_MODE_DET_TREE>(p, tiles_max, st);
-    if (mode == IG_MODE_DET) return launch_one<16, IG_MODE_DET>(p, tiles_max, st);
+    if (mode == IG_MODE_DET) return launch_det<16>(p, tiles_max, st);
     if (mode == IG_MODE_ATOMIC) return launch_one<16, IG_MODE_ATOMIC>(p, tiles_max, st);
     return launch_one<16, IG_MODE_UNSPLIT>(p, tiles_max, st);
   }
   if (mode == IG_MODE_DET_TREE) return launch_one<8, IG_MODE_DET_TREE>(p, tiles_max, st);
-  if (mode == IG_MODE_DET) return launch_one<8, IG_MODE_DET>(p, tiles_max, st);
+  if (mode == IG_MODE_DET) return launch_det<8>(p, tiles_max, st);
   if (mode == IG_MODE_ATOMIC) return launch_one<8, IG_MODE_ATOMIC>(p, tiles_max, st);
   return launch_one<8, IG_MODE_UNSPLIT>(p, tiles_max, st);
 }

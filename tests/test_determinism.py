@@ -355,3 +355,26 @@ def test_batch_invariance_rank16(flags, path):
             assert torch.equal(pz, ref_z[:n]), f"batch {b}"
             assert torch.equal(py, ref_y[:n]), f"batch {b}"
     assert ig.check_status(ws) == 0
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("r", [8, 16, 24])
+def test_lora_shrink_cluster_combine_equals_counter(r, S):
+    """lora_shrink (IG_MODE_DET, warp path) combines the S partitions inside a
+    thread-block cluster where it can (S dividing the tile's outputs, S <=
+    16); IG_FLAG_UNFUSED selects the counter protocol (Algorithm 1). Same
+    partition order, so the same bits; S = 3 always uses the counter."""
+    K = 3096 if S == 3 else 4096          # K/S = 1032 at S = 3: an 8-element last step
+    p = synth.make_problem(90, K, 64, r, slices=2, L=5, seed=r * 100 + S, none_frac=0.1,
+                           device="cuda")
+    zs = []
+    for flags in (0, ig.FLAG_UNFUSED):
+        sh = ig.make_shape(p.M, K, p.N, r, slices=2, num_adapters=5, split_k=S,
+                           mode=ig.MODE_DET, flags=flags)
+        ws = ig.workspace(sh)
+        z = torch.full((2, p.M, r), float("nan"), dtype=torch.float32, device="cuda")
+        ig.lora_shrink(sh, p.x, p.A, p.idx, p.scale, z, ws)
+        assert ig.check_status(ws) == 0
+        zs.append(z)
+    assert torch.equal(zs[0].view(torch.int32), zs[1].view(torch.int32))
+    check_shrink(p.to("cpu"), zs[0])
