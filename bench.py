@@ -328,7 +328,7 @@ def prefill_bench(ig, device, steps):
         u = int(torch.unique(probs[0].idx).numel())
         b = alg_bytes(M, K, N, r, sl, u)
         flops = 2 * M * K * r * sl + 2 * M * r * N * sl
-        res = {"path": "tcgen05" if info["path"] == ig.PATH_MMA else "warp"}
+        res = {"path": "tcgen05" if info["path"] == ig.PATH_MMA else "warp", "split_k": S}
         for part in ("apply", "shrink", "expand"):
             def body(stream, part=part):
                 for p in probs:
