@@ -297,9 +297,10 @@ def kernel_durations(ig, st, ws, steps):
 
 PREFILL = [
     # name, M, K, N, r, slices, L, adapter ids, S, instances
-    # Split-K per shape, the fastest measured of 1 / 2 / 4 / 8 (QKV: apply 82.0 /
-    # 71.3 / 76.6 / 82.8 us; down: 103.4 / 67.9 / 56.2 / 53.4 us)
-    ("qkv_M4096_K4096_r64_3x4096", 4096, 4096, 4096, 64, 3, 16, "segments", 2, 2),
+    # Split-K per shape, the fastest measured of 1 / 2 / 4 / 8 (QKV, slices
+    # stacked in one MMA: apply 114 / 94 / 81 / 74 us; down: 104 / 68 / 56 /
+    # 54 us)
+    ("qkv_M4096_K4096_r64_3x4096", 4096, 4096, 4096, 64, 3, 16, "segments", 8, 2),
     ("down_M4096_K11008_r64_N4096", 4096, 11008, 4096, 64, 1, 16, "segments", 8, 2),
     # Split-K 4 for the large-model shapes: of the allowed 1, 4, 8, 16 the
     # fastest measured (cluster combine, M = 8192: 98 / 110 / 164 us at

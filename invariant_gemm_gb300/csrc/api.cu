@@ -20,7 +20,8 @@ struct Plan {
   int64_t Ks;        // K / S
   int bn;            // shrink rank columns per tile
   int jblocks;       // r / bn
-  int tile_rows;     // rows per tile: 16 (CUDA cores) or 128 (tensor cores)
+  int stack;         // tcgen05 shrink: slices per block (1, or all: MMA N = slices x r)
+  int tile_rows;     // rows per tile: 8 (warp and FMA paths) or 128 (tcgen05)
   int64_t tiles;     // tile-table entries: upper bound on tiles (groups 0..L)
   int ntiles;        // expand column tiles per slice
   size_t off_perm, off_offsets, off_tiles, off_partials, total;
@@ -68,6 +69,11 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   const bool mma = path == IG_PATH_MMA;
   pl->bn = mma ? (int)r : ((r % 16 == 0) ? 16 : 8);
   pl->jblocks = mma ? 1 : (int)(r / pl->bn);
+  // The tcgen05 shrink runs all slices of a tile in one block (one x tile
+  // read, one MMA of N = slices x r) where N fits one MMA; not for the
+  // pairwise-tree mode, whose second launch reads one slice per block.
+  pl->stack = (mma && sh->slices > 1 && sh->slices * r <= 256 &&
+               sh->mode != IG_MODE_DET_TREE) ? sh->slices : 1;
   pl->tile_rows = mma ? kMmaTileRows : kTileRows;
   const int L = sh->num_adapters;
   pl->tiles = tiles_upper_bound(M, L + 1, pl->tile_rows);
@@ -95,8 +101,9 @@ int make_plan(const ig_shape* sh, Plan* pl) {
               !(sh->flags & IG_FLAG_UNFUSED) && fsmem <= 200 * 1024;
 
   uint64_t h = 1469598103934665603ull;
-  const int64_t fields[] = {IG_ABI_VERSION, kArithRevision, path, sh->mode, S, pl->Ks, K, r, N, sh->slices,
-                            pl->bn, mma ? 64 : kShrinkKB, sh->flags & IG_FLAG_Z_FP32};
+  const int64_t fields[] = {IG_ABI_VERSION, kArithRevision, path, sh->mode, S, pl->Ks, K, r, N,
+                            sh->slices, pl->bn, mma ? 64 : kShrinkKB, pl->stack,
+                            sh->flags & IG_FLAG_Z_FP32};
   for (int64_t f : fields) h = fnv1a(h, f);
   pl->key = h;
   return IG_OK;
@@ -157,7 +164,7 @@ int run_shrink_mma(const ig_shape* sh, const Plan& pl, const void* x, const void
                      kMmaTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
-                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)sh->r,
+                     (uint64_t)sh->K, (uint64_t)sh->K * 2, 64, (uint32_t)(pl.stack * sh->r),
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
   p.tiles = reinterpret_cast<const int32_t*>(ws + pl.off_tiles);
@@ -172,6 +179,7 @@ int run_shrink_mma(const ig_shape* sh, const Plan& pl, const void* x, const void
   p.slices = sh->slices;
   p.L = sh->num_adapters;
   p.S = pl.S;
+  p.stack = pl.stack;
   p.flags = sh->flags;
   p.scale = scale;
   return cuda_status(launch_shrink_mma(p, pl.mode, pl.tiles, st));
@@ -416,7 +424,7 @@ int ig_plan_query(const ig_shape* shape, ig_plan_info* out) {
   out->expand_bm = pl.tile_rows;
   out->expand_bn = pl.path == IG_PATH_MMA ? kMmaExpandCols : kExpandBN;
   out->shrink_tiles_max = pl.tiles;
-  out->shrink_ctas_max = pl.tiles * shape->slices * pl.jblocks * pl.S;
+  out->shrink_ctas_max = pl.tiles * (shape->slices / pl.stack) * pl.jblocks * pl.S;
   out->workspace_bytes = (int64_t)pl.total;
   out->determinism_key = pl.key;
   out->apply_kernels = pl.fused ? 1 : 2;

@@ -148,7 +148,7 @@ struct FusedParams {
 struct MmaShrinkParams {
   CUtensorMap tm_x;     // x [M][K], box 64 x 1, 128-byte swizzle (row gathers)
   CUtensorMap tm_xt;    // x [M][K], box 64 x 128, 128-byte swizzle (contiguous tiles)
-  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
+  CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x (stack*r), 128-byte swizzle
   const int32_t* tiles; // 128-row tile table
   float* z;
   float* partials;
@@ -156,6 +156,7 @@ struct MmaShrinkParams {
   uint32_t* status;
   int64_t M, K, r, Ks;
   int32_t slices, L, S, flags;
+  int32_t stack;        // slices per block (1, or all slices: MMA N = slices x r)
   float scale;
 };
 

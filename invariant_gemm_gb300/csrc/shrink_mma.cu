@@ -24,7 +24,10 @@
 // bits, with the partials never leaving the SMs.
 //
 // Block = 4 warps, tile = up to 128 token rows of one adapter (one entry of
-// the token map's 128-row tile table) x all r rank columns. One thread of
+// the token map's 128-row tile table) x all r rank columns of one slice, or of
+// all slices at once where slices x r <= 256 (the slices' A rows are
+// consecutive in A_stack, so one tiled copy and one MMA of N = slices x r
+// serve them, and the x tile is read once instead of once per slice). One thread of
 // warp 0 issues the TMA copies: per k-step of 64 elements, x as one 128-row
 // box when the tile's tokens are consecutive (else row gathers, 4 rows each,
 // only the tile's rows) and one tiled copy of the A block (r rows), all
@@ -70,10 +73,17 @@ struct Ctl {                       // control block at the start of shared memor
   int32_t info[4];
 };
 
-__host__ __device__ inline size_t mma_shrink_smem(int r) {
-  const size_t stage = kXTileBytes + (size_t)r * 128;
+// nc = accumulator columns (stacked slices x r). The cluster combine's
+// receive buffer [S][128/S][nc] FP32 reuses the ring, which is sized to hold
+// it.
+__host__ __device__ inline size_t mma_ring_bytes(int nc, bool cl) {
+  const size_t ring = (size_t)shrink_stages(nc) * (kXTileBytes + (size_t)nc * 128);
+  const size_t recv = (size_t)kMmaTileRows * nc * 4;
+  return cl && recv > ring ? recv : ring;
+}
+__host__ __device__ inline size_t mma_shrink_smem(int nc, bool cl) {
   return 1024 /*align slack*/ + 1024 /*ctl*/ + (size_t)kMmaTileInts * 4 +
-         (size_t)shrink_stages(r) * stage + 1024;
+         mma_ring_bytes(nc, cl) + 1024;
 }
 
 __host__ __device__ inline uint32_t tmem_cols_for(int r) {
@@ -95,16 +105,25 @@ __global__ void __launch_bounds__(kThreads)
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 1024);
   uint8_t* ring = smem + 1024 + ((kMmaTileInts * 4 + 1023) / 1024) * 1024;
   const int r = (int)p.r;
-  const int stage_bytes = kXTileBytes + r * 128;
-  const int nst = shrink_stages(r);
+  const int ns = p.stack;                 // slices of this block
+  const int nc = ns * r;                  // accumulator columns: slice sl0 + c / r, rank c % r
+  const int stage_bytes = kXTileBytes + nc * 128;
+  const int nst = shrink_stages(nc);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
+  const int ngroups = p.slices / ns;
   int64_t bid = blockIdx.x;
   const int s = (int)(bid % S);
   bid /= S;
-  const int sl = (int)(bid % p.slices);
-  const int64_t t = bid / p.slices;
+  const int sg = (int)(bid % ngroups);
+  const int sl0 = sg * ns;
+  const int64_t t = bid / ngroups;
+  // z address of accumulator column c (four columns never straddle a slice:
+  // r is a multiple of 16)
+  auto zrow = [&](int c, int tok) -> float* {
+    return p.z + ((int64_t)(sl0 + c / r) * p.M + tok) * r + c % r;
+  };
 
   for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
   if (tid == 0) {
@@ -116,7 +135,7 @@ __global__ void __launch_bounds__(kThreads)
     if (CL) mbar_init(&ctl->recv, 1);
     fence_mbar_init();
   }
-  const uint32_t ncols = tmem_cols_for(r);
+  const uint32_t ncols = tmem_cols_for(nc);
   if (warp == 1) {
     tmem_alloc(&ctl->tmem, ncols);
     tmem_relinquish();
@@ -128,12 +147,11 @@ __global__ void __launch_bounds__(kThreads)
   const int g = ent_s[0];
   const int nrows = ent_s[1];
   const int32_t* rows_s = ent_s + 4;
-  const int64_t M = p.M;
   // cluster combine: block s owns tile rows [s R, s R + R), R = 128 / S, and
   // receives the S partials of its valid rows
   const int R = kMmaTileRows / S;
   const int own_rows = max(0, min(R, nrows - s * R));
-  if (CL && tid == 0) mbar_arrive_expect_tx(&ctl->recv, (uint32_t)(S * own_rows * r * 4));
+  if (CL && tid == 0) mbar_arrive_expect_tx(&ctl->recv, (uint32_t)(S * own_rows * nc * 4));
 
   auto teardown = [&]() {
     tc_fence_before();
@@ -149,8 +167,7 @@ __global__ void __launch_bounds__(kThreads)
     griddep_wait();
     griddep_launch();
     if (MODE != IG_MODE_ATOMIC && s == 0)
-      for (int i = tid; i < nrows * r; i += kThreads)
-        p.z[((int64_t)sl * M + rows_s[i / r]) * r + i % r] = 0.0f;
+      for (int i = tid; i < nrows * nc; i += kThreads) *zrow(i % nc, rows_s[i / nc]) = 0.0f;
     teardown();
     return;
   }
@@ -158,11 +175,11 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t Ks = p.Ks;
   const int k0 = (int)((int64_t)s * Ks);
   const int nk = (int)((Ks + kKStep - 1) / kKStep);      // k-steps
-  const int a_row = (int)(((int64_t)g * p.slices + sl) * r);
+  const int a_row = (int)(((int64_t)g * p.slices + sl0) * r);
   const int groups4 = (nrows + 3) / 4;
   const bool contiguous = ent_s[2] != 0;   // rows are consecutive tokens: one box
   const uint32_t stage_tx =
-      (contiguous ? (uint32_t)kXTileBytes : (uint32_t)groups4 * 4 * 128) + (uint32_t)r * 128;
+      (contiguous ? (uint32_t)kXTileBytes : (uint32_t)groups4 * 4 * 128) + (uint32_t)nc * 128;
   const bool early_a = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
   const int first = min(nk, nst);
 
@@ -211,7 +228,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
-    const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, r);
+    const uint32_t idesc = umma_idesc_bf16_f32(kMmaTileRows, nc);
     for (int b = 0; b < nk; ++b) {
       const int st = b % nst;
       if (!mbar_wait_bounded(&ctl->full[st], (uint32_t)((b / nst) & 1), p.status)) {
@@ -241,19 +258,19 @@ __global__ void __launch_bounds__(kThreads)
     // Every block's MMAs are complete (so its ring is free) once the cluster
     // barrier returns. Each thread then sends its accumulator row to the
     // owner of the row, into slot s of the owner's receive buffer
-    // [S][R][r] FP32 (the ring), counted on the owner's mbarrier. Every block
+    // [S][R][nc] FP32 (the ring), counted on the owner's mbarrier. Every block
     // sends on every path, so every owner receives all its bytes.
     fence_proxy_async_smem();
     cluster_sync_all();
     float* recv = reinterpret_cast<float*>(ring);
     const int q = row / R, lr = row % R;
     const uint32_t dst_bar = map_rank(&ctl->recv, (uint32_t)q);
-    for (int c = 0; c < r; c += 32) {
+    for (int c = 0; c < nc; c += 32) {
       float v[32];
       tmem_ld32(trow + c, v);
       if (row >= nrows) continue;
-      const int nv = min(32, r - c);   // r is a multiple of 16
-      const uint32_t dst = map_rank(recv + ((size_t)s * R + lr) * r + c, (uint32_t)q);
+      const int nv = min(32, nc - c);   // nc is a multiple of 16
+      const uint32_t dst = map_rank(recv + ((size_t)s * R + lr) * nc + c, (uint32_t)q);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (4 * i < nv)
@@ -265,19 +282,19 @@ __global__ void __launch_bounds__(kThreads)
     const bool got = mbar_wait_bounded(&ctl->recv, 0, p.status, 1ll << 36);
     // Combine (Algorithm 1 order) of the owned rows: total = 0; total += P_q
     // for q = 0..S-1; z = total * scale. Four columns per step.
-    const int n4 = own_rows * r / 4;
+    const int n4 = own_rows * nc / 4;
     const float4* rv = reinterpret_cast<const float4*>(recv);
     for (int o4 = tid; got && acc_ok && o4 < n4; o4 += kThreads) {
       float4 total = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       for (int q2 = 0; q2 < S; ++q2) {
-        const float4 v = rv[q2 * (R * r / 4) + o4];
+        const float4 v = rv[q2 * (R * nc / 4) + o4];
         total.x += v.x;
         total.y += v.y;
         total.z += v.z;
         total.w += v.w;
       }
       const int o = 4 * o4;
-      *reinterpret_cast<float4*>(p.z + ((int64_t)sl * M + rows_s[s * R + o / r]) * r + o % r) =
+      *reinterpret_cast<float4*>(zrow(o % nc, rows_s[s * R + o / nc])) =
           make_float4(total.x * p.scale, total.y * p.scale, total.z * p.scale,
                       total.w * p.scale);
     }
@@ -288,33 +305,30 @@ __global__ void __launch_bounds__(kThreads)
     teardown();
     return;
   }
-  const int64_t slot = t * p.slices + sl;
-  float* part = p.partials + slot * (int64_t)S * (kMmaTileRows * r);
-  for (int c = 0; c < r; c += 32) {
+  const int64_t slot = t * ngroups + sg;
+  float* part = p.partials + slot * (int64_t)S * (kMmaTileRows * nc);
+  for (int c = 0; c < nc; c += 32) {
     float v[32];
     tmem_ld32(trow + c, v);
     if (!acc_ok || row >= nrows) continue;
-    const int nv = min(32, r - c);   // r is a multiple of 16
+    const int nv = min(32, nc - c);   // nc is a multiple of 16
     if (MODE == IG_MODE_DET || MODE == IG_MODE_DET_TREE) {
-      float4* dst = reinterpret_cast<float4*>(part + (int64_t)s * (kMmaTileRows * r) +
-                                              (int64_t)row * r + c);
+      float4* dst = reinterpret_cast<float4*>(part + (int64_t)s * (kMmaTileRows * nc) +
+                                              (int64_t)row * nc + c);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (4 * i < nv) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else if (MODE == IG_MODE_UNSPLIT) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (4 * i < nv)
+          *reinterpret_cast<float4*>(zrow(c + 4 * i, rows_s[row])) =
+              make_float4(v[4 * i] * p.scale, v[4 * i + 1] * p.scale, v[4 * i + 2] * p.scale,
+                          v[4 * i + 3] * p.scale);
     } else {
-      float* zp = p.z + ((int64_t)sl * M + rows_s[row]) * r + c;
-      if (MODE == IG_MODE_UNSPLIT) {
-        float4* z4 = reinterpret_cast<float4*>(zp);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (4 * i < nv)
-            z4[i] = make_float4(v[4 * i] * p.scale, v[4 * i + 1] * p.scale,
-                                v[4 * i + 2] * p.scale, v[4 * i + 3] * p.scale);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nv) atomicAdd(zp + i, v[i] * p.scale);
-      }
+      for (int i = 0; i < 32; ++i)
+        if (i < nv) atomicAdd(zrow(c + i, rows_s[row]), v[i] * p.scale);
     }
   }
 
@@ -333,14 +347,14 @@ __global__ void __launch_bounds__(kThreads)
       // one row) and adds the partitions q = 0..S-1 in order; the 16 loads of
       // one partition are in flight together.
       constexpr int kPer = 16;
-      const int n4 = nrows * r / 4;
+      const int n4 = nrows * nc / 4;
       for (int base = 0; base < n4; base += kPer * kThreads) {
         float4 tot[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; ++i) tot[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         for (int q = 0; q < S; ++q) {
           const float4* src =
-              reinterpret_cast<const float4*>(part + (int64_t)q * (kMmaTileRows * r));
+              reinterpret_cast<const float4*>(part + (int64_t)q * (kMmaTileRows * nc));
           float4 v[kPer];
 #pragma unroll
           for (int i = 0; i < kPer; ++i) {
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(kThreads)
           const int o4 = base + i * kThreads + tid;
           if (o4 >= n4) continue;
           const int o = 4 * o4;
-          *reinterpret_cast<float4*>(p.z + ((int64_t)sl * M + rows_s[o / r]) * r + o % r) =
+          *reinterpret_cast<float4*>(zrow(o % nc, rows_s[o / nc])) =
               make_float4(tot[i].x * p.scale, tot[i].y * p.scale, tot[i].z * p.scale,
                           tot[i].w * p.scale);
         }
@@ -381,26 +395,27 @@ __global__ void __launch_bounds__(kThreads)
 template <int MODE>
 cudaError_t launch_mode(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
   auto kern = shrink_mma_kernel<MODE, false>;
-  const size_t smem = mma_shrink_smem((int)p.r);
+  const size_t smem = mma_shrink_smem((int)(p.stack * p.r), false);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  const int64_t grid = tiles_max * p.slices * p.S;
+  const int64_t grid = tiles_max * (p.slices / p.stack) * p.S;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
 }
 
-// Can a cluster of S blocks of this size be resident? Cached per (S, r).
-bool cluster_fits(int S, int r) {
+// Can a cluster of S blocks with this footprint be resident? Cached per
+// (S, accumulator columns).
+bool cluster_fits(int S, int nc) {
   static std::mutex mu;
   static std::map<std::pair<int, int>, bool> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(S, r);
+  const auto key = std::make_pair(S, nc);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   auto kern = shrink_mma_kernel<IG_MODE_DET, true>;
-  const size_t smem = mma_shrink_smem(r);
+  const size_t smem = mma_shrink_smem(nc, true);
   bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) == cudaSuccess;
   if (ok && S > 8)
@@ -428,7 +443,7 @@ bool cluster_fits(int S, int r) {
 
 cudaError_t launch_cluster(const MmaShrinkParams& p, int64_t tiles_max, cudaStream_t st) {
   auto kern = shrink_mma_kernel<IG_MODE_DET, true>;
-  const size_t smem = mma_shrink_smem((int)p.r);
+  const size_t smem = mma_shrink_smem((int)(p.stack * p.r), true);
   // per launch: the attribute is per function, and other ranks set it too
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -437,7 +452,7 @@ cudaError_t launch_cluster(const MmaShrinkParams& p, int64_t tiles_max, cudaStre
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  const int64_t grid = tiles_max * p.slices * p.S;
+  const int64_t grid = tiles_max * (p.slices / p.stack) * p.S;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -466,12 +481,11 @@ cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_
   if (mode == IG_MODE_DET) {
     // the cluster combine and the counter protocol give the same bits
     // (rows are dealt to the S blocks in equal shares, S must divide 128; the
-    // received partials, 128 rows x r FP32, live in the copy ring)
-    const int r = (int)p.r;
-    const bool recv_fits = (size_t)kMmaTileRows * r * 4 <=
-                           (size_t)shrink_stages(r) * (kXTileBytes + (size_t)r * 128);
-    if (!(p.flags & IG_FLAG_UNFUSED) && p.S <= 16 && kMmaTileRows % p.S == 0 && recv_fits &&
-        cluster_fits(p.S, r))
+    // received partials, 128 rows x nc FP32, share the ring's memory, and the
+    // footprint must leave two blocks per SM)
+    const int nc = (int)(p.stack * p.r);
+    if (!(p.flags & IG_FLAG_UNFUSED) && p.S <= 16 && kMmaTileRows % p.S == 0 &&
+        mma_ring_bytes(nc, true) <= 110 * 1024 && cluster_fits(p.S, nc))
       return launch_cluster(p, tiles_max, st);
     return launch_mode<IG_MODE_DET>(p, tiles_max, st);
   }
