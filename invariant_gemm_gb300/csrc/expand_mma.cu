@@ -32,7 +32,9 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kBN = kMmaExpandBN;                // output columns per column block
-constexpr int kYBytes = kMmaTileRows * 128;      // y tile of one column block (16 KB)
+constexpr int kYB = kBN / 64;                    // 64-column y boxes per column block
+constexpr int kYBox = kMmaTileRows * 128;        // one y box: 128 rows x 64 columns (16 KB)
+constexpr int kYBytes = kYB * kYBox;             // y tile of one column block
 constexpr int kBAtom = kBN * 128;                // B rows of one column block, per 64 ranks
 
 constexpr int kMaxStages = 3;
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kThreads)
   const bool contiguous = ent_s[2] != 0;   // rows are consecutive tokens: one box
   const bool full_box = contiguous && nrows == kMmaTileRows;
   const bool early_b = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
-  const uint32_t y_tx = contiguous ? (uint32_t)kYBytes : (uint32_t)groups4 * 4 * 128;
+  const uint32_t y_tx = kYB * (contiguous ? (uint32_t)kYBox : (uint32_t)groups4 * 4 * 128);
 
   // column block i: stage i % NS (phase (i / NS) & 1), accumulator i % 2
   // (phase (i / 2) & 1)
@@ -154,14 +156,20 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) mbar_arrive_expect_tx(&ctl->full_y[i % NS], y_tx);
     __syncwarp();
     if (contiguous) {
-      if (lane == 0) tma_load_2d(sy, &p.tm_yt, y_col + i * kBN, rows_s[0], &ctl->full_y[i % NS]);
+      if (lane == 0)
+        for (int yb = 0; yb < kYB; ++yb)
+          tma_load_2d(sy + yb * kYBox, &p.tm_yt, y_col + i * kBN + yb * 64, rows_s[0],
+                      &ctl->full_y[i % NS]);
       return;
     }
     const int last = nrows - 1;
-    for (int q = lane; q < groups4; q += 32)
-      tma_gather4(sy + q * 512, &p.tm_y, y_col + i * kBN, rows_s[min(4 * q, last)],
-                  rows_s[min(4 * q + 1, last)], rows_s[min(4 * q + 2, last)],
-                  rows_s[min(4 * q + 3, last)], &ctl->full_y[i % NS]);
+    for (int q = lane; q < groups4 * kYB; q += 32) {
+      const int yb = q / groups4, g4 = q % groups4;
+      tma_gather4(sy + yb * kYBox + g4 * 512, &p.tm_y, y_col + i * kBN + yb * 64,
+                  rows_s[min(4 * g4, last)], rows_s[min(4 * g4 + 1, last)],
+                  rows_s[min(4 * g4 + 2, last)], rows_s[min(4 * g4 + 3, last)],
+                  &ctl->full_y[i % NS]);
+    }
   };
 
   if (tid == 0 && early_b)
@@ -271,10 +279,10 @@ __global__ void __launch_bounds__(kThreads)
         float v[32];
         tmem_ld32(trow + c, v);
         if (m >= nrows) continue;
-        uint8_t* rowp = sy + m * 128;
+        uint8_t* rowp = sy + (c / 64) * kYBox + m * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int chunk = c / 8 + q;                       // logical 16-byte chunk
+          const int chunk = (c % 64) / 8 + q;                // logical 16-byte chunk
           uint4* cp = reinterpret_cast<uint4*>(rowp + ((chunk ^ (m & 7)) * 16));
           uint4 u = *cp;
           float yf[8];
@@ -298,18 +306,22 @@ __global__ void __launch_bounds__(kThreads)
     const int ncols = (int)min((int64_t)kBN, N - n0 - (int64_t)i * kBN);
     if (full_box && ncols == kBN) {
       if (tid == 0) {
-        tma_store_2d(&p.tm_yt, y_col + i * kBN, rows_s[0], sy);
+        for (int yb = 0; yb < kYB; ++yb)
+          tma_store_2d(&p.tm_yt, y_col + i * kBN + yb * 64, rows_s[0], sy + yb * kYBox);
         bulk_commit();
       }
     } else {
-      // four rows (128 bytes each) per warp-instruction
-      for (int m0 = 4 * warp; m0 < nrows; m0 += 16) {
-        const int m = m0 + lane / 8;
-        const int ch = lane % 8;              // 16-byte chunk of the 128-byte row
-        if (m >= nrows || ch * 8 >= ncols) continue;
-        const uint4 u = *reinterpret_cast<const uint4*>(sy + m * 128 + ((ch ^ (m & 7)) * 16));
-        *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + ch * 8) = u;
-      }
+      // four rows (128 bytes of one 64-column box each) per warp-instruction
+      for (int yb = 0; yb < kYB; ++yb)
+        for (int m0 = 4 * warp; m0 < nrows; m0 += 16) {
+          const int m = m0 + lane / 8;
+          const int ch = lane % 8;              // 16-byte chunk of the 128-byte row
+          if (m >= nrows || yb * 64 + ch * 8 >= ncols) continue;
+          const uint4 u = *reinterpret_cast<const uint4*>(sy + yb * kYBox + m * 128 +
+                                                          ((ch ^ (m & 7)) * 16));
+          *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + yb * 64 +
+                                    ch * 8) = u;
+        }
     }
     __syncthreads();
     // stage i % NS is free once the store has read it: copies of block i + NS
