@@ -78,7 +78,7 @@ struct MapParams {
   int64_t M;
   int64_t tiles_max;
   int32_t L;
-  int32_t tile_rows;   // 16 (CUDA-core path) or 128 (tensor-core path)
+  int32_t tile_rows;   // 8 (warp and FMA paths) or 128 (tcgen05 path)
 };
 
 struct ShrinkParams {

@@ -19,8 +19,8 @@
 //
 // Finally it writes the tile table the shrink and expand kernels read: group
 // g is cut into ceil(count_g / T) tiles of at most T consecutive rows of the
-// grouped order (T = 8 for the CUDA-core kernels, 128 for the tensor-core
-// ones); tile entries hold [g, nrows, contiguous, 0, rows[T]] so that a block
+// grouped order (T = 8 for the warp-path and FMA-path kernels, 128 for the tcgen05
+// kernels); tile entries hold [g, nrows, contiguous, 0, rows[T]] so that a block
 // learns its adapter and its token rows with one contiguous load.
 // `contiguous` is 1 when the rows are consecutive token indices (then a
 // tile can be copied as one box instead of row by row). Tiles of
