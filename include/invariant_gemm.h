@@ -99,11 +99,15 @@ typedef enum ig_mode {
 /* Arithmetic path. It is part of the determinism key: the same request on
  * another path gives results within tolerance but not bit-equal. */
 typedef enum ig_path {
-  IG_PATH_AUTO = 0,  /* chosen from (K, r, N, slices) only, never from M */
+  IG_PATH_AUTO = 0,  /* chosen from (K, r, N, slices, flags) only, never
+                        from M: IG_PATH_MMA for r >= 32 where it applies,
+                        else IG_PATH_WARP */
   IG_PATH_WARP = 1,  /* small ranks: 8-token tiles on the warp-level tensor
                         cores (bf16 mma.sync m16n8k16, FP32 accumulation) */
   IG_PATH_MMA = 2,   /* 128-token tiles on the tcgen05 tensor cores, FP32
-                        accumulation in TMEM */
+                        accumulation in TMEM; needs r and K/S multiples of
+                        16, and r <= 192 with IG_FLAG_Z_FP32
+                        (IG_ERR_UNSUPPORTED otherwise) */
   IG_PATH_FMA = 3    /* small ranks on CUDA cores: 8-token tiles, FP32 FMA in
                         increasing k per lane, warp-shuffle butterfly across
                         lanes; never chosen by IG_PATH_AUTO (the warp path
@@ -143,13 +147,12 @@ typedef struct ig_shape {
 #define IG_FLAG_Z_FP32 4         /* The expand reads Z in FP32 instead of
                                     rounding it to bf16 first (sec. 6.2 shows
                                     the bf16 boundary turning tiny FP32
-                                    differences into visible ones). Warp
-                                    path: Z = hi + mid + lo exactly (three
-                                    bf16 parts, three MMAs per j chunk).
-                                    tcgen05 path: Z = hi + lo with hi =
-                                    bf16_rn(Z), lo = bf16_rn(Z - hi), two
-                                    MMAs per K step (16 significant bits of
-                                    Z). */
+                                    differences into visible ones). Tensor-
+                                    core paths: Z = hi + mid + lo exactly,
+                                    hi = bf16_rn(Z), mid = bf16_rn(Z - hi),
+                                    lo = bf16_rn(Z - hi - mid), three MMAs
+                                    per step of the rank sum; FMA path: Z
+                                    used as stored. */
 
 /* The resolved plan. Everything that fixes the arithmetic is in
  * determinism_key, which never depends on M. */
@@ -216,8 +219,8 @@ int lora_shrink(const ig_shape* shape, const void* x, const void* A_stack,
 /* Expand (Eq. 1, sec. 6.2):
  *   y[m][sl*N + n] = bf16_rn( f32(y[m][sl*N+n])
  *                             + sum_{j<r} bf16_rn(z[sl][m][j]) * B_stack[a_m][sl][n][j] )
- * (with IG_FLAG_Z_FP32: z[sl][m][j] itself, or its hi/lo bf16 pair on the
- * tensor-core path, instead of bf16_rn(z))
+ * (with IG_FLAG_Z_FP32: z[sl][m][j] itself instead of bf16_rn(z); the
+ * tensor-core paths feed it as three bf16 parts that sum to it exactly)
  * The sum over j is a sequential FP32 chain in increasing j; y is rounded
  * once. Rows with adapter -1 are not written. adapter_idx may be NULL to
  * reuse the token map in ws. */

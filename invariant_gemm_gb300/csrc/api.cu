@@ -57,7 +57,11 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   // Tensor cores where the token x rank x K tile is a dense contraction:
   // ranks of 32 and more (prefill-class adapters). Decided from r and K/S,
   // never from M.
-  const bool mma_ok = r % 16 == 0 && (K / S) % 16 == 0 && r <= 256;
+  // With FP32 Z the tcgen05 expand keeps three bf16 parts of the tile's Z in
+  // shared memory, which for r = 256 no longer fits beside its copy stages.
+  const bool mma_ok = r % 16 == 0 && (K / S) % 16 == 0 && r <= 256 &&
+                      expand_mma_smem_bytes((int)r, (sh->flags & IG_FLAG_Z_FP32) != 0) <=
+                          227 * 1024;
   int path = sh->path;
   if (path == IG_PATH_AUTO) path = (mma_ok && r >= 32) ? IG_PATH_MMA : IG_PATH_WARP;
   if (path == IG_PATH_MMA && !mma_ok) return IG_ERR_UNSUPPORTED;

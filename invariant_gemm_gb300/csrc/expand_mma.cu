@@ -59,7 +59,7 @@ __host__ __device__ inline size_t stage_bytes(int r) {
   return (size_t)((r + 63) / 64) * kBAtom + kYBytes;
 }
 __host__ __device__ inline size_t off_stage(int r, bool zf32, int s) {
-  return off_zb() + (size_t)((r + 63) / 64) * 16384 * (zf32 ? 2 : 1) + s * stage_bytes(r);
+  return off_zb() + (size_t)((r + 63) / 64) * 16384 * (zf32 ? 3 : 1) + s * stage_bytes(r);
 }
 __host__ __device__ inline size_t mma_expand_smem(int r, bool zf32) {
   return 1024 + off_stage(r, zf32, expand_stages(r));
@@ -186,8 +186,9 @@ __global__ void __launch_bounds__(kThreads)
   // A operand: the tile's Z rows rounded to bf16 into the swizzled K-major
   // layout (16-byte chunk c of a 128-byte row m sits at chunk c ^ (m % 8)),
   // rows past nrows zero. Warp w loads rows 32w .. 32w+31, r/4 lanes per row
-  // (4 values each, coalesced). With FP32 Z also the remainder
-  // lo = bf16_rn(z - hi), in atoms after the hi ones.
+  // (4 values each, coalesced). With FP32 Z also mid = bf16_rn(z - hi) and
+  // lo = bf16_rn(z - hi - mid) (hi + mid + lo == z exactly), in atoms after
+  // the hi ones.
   {
     const int per_row = r / 4;
     for (int idx = lane; idx < 32 * per_row; idx += 32) {
@@ -196,18 +197,20 @@ __global__ void __launch_bounds__(kThreads)
       float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (m < nrows) f = __ldcg(reinterpret_cast<const float4*>(p.z + ((int64_t)sl * M + rows_s[m]) * r + j));
       const float fv[4] = {f.x, f.y, f.z, f.w};
-      uint32_t hi[4], lo[4];
+      uint32_t pt[3][4];   // bf16 parts hi, mid, lo
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        hi[e] = f32_to_bf16_bits(fv[e]);
-        lo[e] = zf32 ? f32_to_bf16_bits(fv[e] - __uint_as_float(hi[e] << 16)) : 0u;
+        uint16_t h, md, l;
+        split_z(fv[e], zf32, h, md, l);
+        pt[0][e] = h;
+        pt[1][e] = md;
+        pt[2][e] = l;
       }
       const int a = j / 64, c = (j % 64) / 8;
       const size_t off = (size_t)a * 16384 + m * 128 + ((c ^ (m & 7)) << 4) + (j % 8) * 2;
-      *reinterpret_cast<uint2*>(s_zb + off) = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-      if (zf32)
-        *reinterpret_cast<uint2*>(s_zb + (size_t)ka * 16384 + off) =
-            make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+      for (int q = 0; q < (zf32 ? 3 : 1); ++q)
+        *reinterpret_cast<uint2*>(s_zb + (size_t)q * ka * 16384 + off) =
+            make_uint2(pt[q][0] | (pt[q][1] << 16), pt[q][2] | (pt[q][3] << 16));
     }
     // rank columns past r inside the last atom are zero
     if (r % 64) {
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kThreads)
         const int m = idx / ((64 - r % 64) / 8);
         const int c = (r % 64) / 8 + idx % ((64 - r % 64) / 8);
         const size_t off = (size_t)(ka - 1) * 16384 + m * 128 + ((c ^ (m & 7)) << 4);
-        *reinterpret_cast<uint4*>(s_zb + off) = make_uint4(0u, 0u, 0u, 0u);
-        if (zf32) *reinterpret_cast<uint4*>(s_zb + (size_t)ka * 16384 + off) = make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < (zf32 ? 3 : 1); ++q)
+          *reinterpret_cast<uint4*>(s_zb + (size_t)q * ka * 16384 + off) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
@@ -236,9 +239,10 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t bdesc = umma_desc_sw128(sb + a * kBAtom + kk * 32);
         umma_bf16(acc, umma_desc_sw128(smem_u32(s_zb + a * 16384) + kk * 32), bdesc, idesc,
                   k > 0);
-        if (zf32)
-          umma_bf16(acc, umma_desc_sw128(smem_u32(s_zb + (ka + a) * 16384) + kk * 32), bdesc,
-                    idesc, true);
+        if (zf32)   // mid and lo parts of FP32 Z, same k step
+          for (int q = 1; q < 3; ++q)
+            umma_bf16(acc, umma_desc_sw128(smem_u32(s_zb + (q * ka + a) * 16384) + kk * 32),
+                      bdesc, idesc, true);
       }
     } else {
       ctl->fail = 1;
@@ -368,6 +372,6 @@ cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaS
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
 }
 
-size_t expand_mma_smem_bytes(int r) { return mma_expand_smem(r, false); }
+size_t expand_mma_smem_bytes(int r, bool z_fp32) { return mma_expand_smem(r, z_fp32); }
 
 }  // namespace ig

@@ -54,7 +54,7 @@ constexpr int kExpandBN = 256;        // output columns per expand block: 4 warp
 // copy layout only: results do not depend on it).
 constexpr int64_t kXWideMinM = 128;
 // Revision of the arithmetic of the kernels; part of the determinism key.
-constexpr int kArithRevision = 2;
+constexpr int kArithRevision = 3;
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
@@ -203,7 +203,7 @@ int expand_warp_box_rows(int r, int64_t N);
 cudaError_t launch_shrink_mma(const MmaShrinkParams& p, int mode, int64_t tiles_max,
                               cudaStream_t st);
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st);
-size_t expand_mma_smem_bytes(int r);
+size_t expand_mma_smem_bytes(int r, bool z_fp32);
 cudaError_t launch_reduce_tree(const TreeParams& p, int64_t tiles_max, cudaStream_t st);
 
 // Launch helper: programmatic dependent launch on `st` (see griddep_wait).
@@ -342,6 +342,24 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote, float4 v, uint32_t 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Z split for the expand's A operand: hi = bf16(z); with full FP32 Z also
+// mid = bf16(z - hi) and lo = bf16(z - hi - mid), each difference exact, so
+// that hi + mid + lo == z exactly (24 significant bits = 3 x 8).
+__device__ __forceinline__ void split_z(float z, bool fp32, uint16_t& hi, uint16_t& mid,
+                                        uint16_t& lo) {
+  const uint32_t h = f32_to_bf16_bits(z);
+  hi = (uint16_t)h;
+  if (!fp32) {
+    mid = lo = 0;
+    return;
+  }
+  const float r1 = z - __uint_as_float(h << 16);
+  const uint32_t m = f32_to_bf16_bits(r1);
+  const float r2 = r1 - __uint_as_float(m << 16);
+  mid = (uint16_t)m;
+  lo = (uint16_t)f32_to_bf16_bits(r2);
 }
 
 // Fetch a kernel-parameter tensor map into the descriptor cache early.

@@ -70,24 +70,6 @@ __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1
 // Round-to-nearest-even bf16 bits of an FP32 value, as the low half.
 __device__ __forceinline__ uint32_t bf16_bits(float f) { return f32_to_bf16_bits(f); }
 
-// Z split for the expand's A operand: hi = bf16(z); with full FP32 Z also
-// mid = bf16(z - hi) and lo = bf16(z - hi - mid), each difference exact, so
-// that hi + mid + lo == z exactly (24 significant bits = 3 x 8).
-__device__ __forceinline__ void split_z(float z, bool fp32, uint16_t& hi, uint16_t& mid,
-                                        uint16_t& lo) {
-  const uint32_t h = bf16_bits(z);
-  hi = (uint16_t)h;
-  if (!fp32) {
-    mid = lo = 0;
-    return;
-  }
-  const float r1 = z - __uint_as_float(h << 16);
-  const uint32_t m = bf16_bits(r1);
-  const float r2 = r1 - __uint_as_float(m << 16);
-  mid = (uint16_t)m;
-  lo = (uint16_t)bf16_bits(r2);
-}
-
 // One 8-column block of the expand on the tensor cores:
 //   D[m][n] = sum over j of Zb[m][j] * B[cb + n][j],  m < 8 (rows 8..15 zero)
 // j in increasing 16-element chunks (an 8-element chunk last when r % 16 ==

@@ -110,11 +110,21 @@ def test_workspace_bytes():
     (dict(M=-1), -2), (dict(mode=4), -1), (dict(path=7), -1),
     (dict(num_adapters=5000), -9), (dict(r=512), -9),
     (dict(mode=3, split_k=128), -9),
+    (dict(r=256, path=2, flags=4), -9),        # three bf16 Z parts do not fit at r = 256
 ])
 def test_plan_rejects(kw, code):
     with pytest.raises(ig.IGError) as e:
         ig.plan_query(shp(**kw))
     assert e.value.code == code
+
+
+def test_fp32_z_large_rank_plan():
+    """With FP32 Z the tcgen05 expand holds three bf16 parts of a 128-row Z tile;
+    up to r = 192 they fit beside its copy stages, at r = 256 the automatic plan
+    takes the warp path instead."""
+    assert ig.plan_query(shp(r=192, flags=ig.FLAG_Z_FP32))["path"] == ig.PATH_MMA
+    assert ig.plan_query(shp(r=256))["path"] == ig.PATH_MMA
+    assert ig.plan_query(shp(r=256, flags=ig.FLAG_Z_FP32))["path"] == ig.PATH_WARP
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first

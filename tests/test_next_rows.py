@@ -148,7 +148,8 @@ def check_expand_fp32(prob, z_gpu, y_gpu):
 
 
 @pytest.mark.parametrize("r,path", [(16, ig.PATH_WARP), (64, ig.PATH_MMA), (32, ig.PATH_WARP),
-                                    (24, ig.PATH_WARP)])
+                                    (24, ig.PATH_WARP), (192, ig.PATH_MMA), (80, ig.PATH_MMA),
+                                    (256, ig.PATH_AUTO)])
 def test_fp32_z_expand(r, path):
     p = synth.make_problem(120, 4096, 520, r, slices=2, L=3, seed=r, none_frac=0.1,
                            device="cuda")
