@@ -26,13 +26,17 @@
 // Block = r/4 warps; cluster = S blocks (rank s = K partition s); tile = up
 // to 8 token rows of one adapter (tile-table entry) x all r rank columns
 // (r = 8 or 16). Copies: per 64-element sub-block the A rows by one tiled TMA
-// copy and the token rows of x by row-gather TMA copies (4 rows each); the
-// block's B column slice by tiled TMA copies of 128-byte rows (64/r columns
-// x r ranks each); all 128-byte swizzled, so that ldmatrix reads of 8 rows
-// hit 8 distinct bank groups. The y values a lane will update are loaded into
-// registers right after griddep_wait, so they arrive while the shrink
-// computes. Both the shrink partial and the expand run on the warp-level
-// tensor cores (warp_mma.cuh).
+// copy and the token rows of x by row-gather TMA copies (4 rows each), the
+// first k-blocks issued by different warps (a TMA copy issued after
+// griddepcontrol.wait took a few hundred ns to leave its warp on GB300, so
+// one warp issuing them all serialised them); the block's B column slice by
+// tiled TMA copies of 128-byte rows (64/r columns x r ranks each); all
+// 128-byte swizzled, so that ldmatrix reads of 8 rows hit 8 distinct bank
+// groups. Before griddep_wait, L2 is asked for the block's x and y rows
+// (0.3 us per layer at 256 tokens). The y values a lane will update are
+// loaded into registers right after the x copies are issued, so they arrive
+// while the shrink computes. Both the shrink partial and the expand run on
+// the warp-level tensor cores (warp_mma.cuh).
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -144,7 +148,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   pa.nrows = nrows;
   pa.tm_x = &p.tm_x;
   pa.tm_xs = &p.tm_xs;
-  pa.wide_rows = p.x_wide_rows;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)((int64_t)s * p.Ks);
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   ring.nst = lay.nst;
   ring.nkb = (int)((p.Ks + kShrinkKB - 1) / kShrinkKB);
   const int first = min(ring.nkb, lay.nst);
+  pa.wide_rows = p.x_wide_rows;
 
   // B rows of this block: 128-byte row u holds columns c0 + CU*u .. + CU-1
   const int b_row0 = (int)((((int64_t)g * p.slices + sl) * N + c0) / CU);
@@ -174,29 +178,41 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
       if (early_w) ring.issue_a(pa, b);
     }
     if (early_w) issue_b();
+  } else if (warp == 1) {
+    // Ask L2 for this block's x and y rows now. A prefetch has no effect on
+    // the values read: the loads after griddep_wait() see the previous
+    // kernel's writes, L2 being where they land.
+    if (lane < nrows)
+      bulk_prefetch_l2(p.x + (int64_t)rows_s[lane] * p.K + pa.k0, (uint32_t)(p.Ks * 2));
+    else if (lane >= 8 && lane - 8 < nrows && ncols > 0)
+      bulk_prefetch_l2(p.y + (int64_t)rows_s[lane - 8] * ((int64_t)p.slices * N) +
+                           (int64_t)sl * N + c0,
+                       (uint32_t)(ncols * 2));
   }
   griddep_wait();
   griddep_launch();
-  if (warp == 0) {
-    for (int b = 0; b < first; ++b) {
-      if (!early_w) ring.issue_a(pa, b);
-      ring.issue_x(pa, b);
-    }
-    if (!early_w) issue_b();
+  if (warp == 0 && !early_w) {
+    for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
+    issue_b();
   }
-
   // Expand geometry: warp w takes the 8-column blocks w, w + W, ...; lane
   // 4g + t updates row g, columns 2t and 2t+1 of each (one bf16 pair of y).
-  // Its first kPre pairs are loaded now and arrive during the shrink.
+  // Its first kPre pairs are loaded right after the x copies are issued and
+  // arrive during the shrink.
   const int gq = lane >> 2, tq = lane & 3;
   const bool has_row = gq < nrows;
   __nv_bfloat16* yrow = p.y + (int64_t)rows_s[min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
                         (int64_t)sl * N + c0 + 2 * tq;
   uint32_t ypre[kPre];
+  auto load_ypre = [&]() {
 #pragma unroll
-  for (int i = 0; i < kPre; ++i)
-    if (has_row && warp + i * W < nblk)
-      ypre[i] = *reinterpret_cast<const uint32_t*>(yrow + (warp + i * W) * 8);
+    for (int i = 0; i < kPre; ++i)
+      if (has_row && warp + i * W < nblk)
+        ypre[i] = *reinterpret_cast<const uint32_t*>(yrow + (warp + i * W) * 8);
+  };
+  // one k-block per warp, so that the copies leave the warps in parallel
+  for (int b = warp; b < first; b += W) ring.issue_x(pa, b);
+  load_ypre();
 
   float v;
   const bool ok = ring.run(pa, v);

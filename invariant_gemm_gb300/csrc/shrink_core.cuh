@@ -139,20 +139,99 @@ struct PartialRing {
     }
   }
 
-  // All threads. The first min(nkb, nst) k-blocks must already be armed and
-  // issued. On return `out` is this thread's output: token row tid / BN,
-  // rank tid % BN (not yet scaled). Returns false if a copy wait expired
-  // (after draining, bounded, every copy still in flight).
-  __device__ __forceinline__ bool run(const PartialArgs& a, float& out) const {
+  // The MMAs of k-block b (stage st, kl elements) for this warp, accumulated
+  // into d: 16-element steps kk = warp, warp + W, ... in increasing order, the
+  // last 8 elements (kl % 16 == 8) by the warp whose turn it is.
+  __device__ __forceinline__ void mma_kblock(const PartialArgs& a, int st, int kl,
+                                             float (&d)[4]) const {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     // ldmatrix row addresses of this lane: A (ranks) rows and x (tokens) rows
     const int arow = (lane & 7) + (BN == 16 ? 8 * ((lane >> 3) & 1) : 0);
     const int achunk = BN == 16 ? (lane >> 4) : ((lane >> 3) & 1);
     const int xrow = min(lane & 7, a.nrows - 1);   // this lane's token row
     const int xchunk = (lane >> 3) & 1;
     const bool wd = wide(a);
+    const int n16 = kl / 16;
+    const uint32_t sx = smem_u32(stages + st * kStageBytes);
+    const uint32_t sa = sx + kXBytes;
+    // operands of step kk (16 elements): A fragment (ranks) and x fragment (tokens)
+    auto frag = [&](int kk, uint32_t (&af)[4], uint32_t (&bf)[2]) {
+      const int q = kk >> 2, c16 = (kk & 3) * 2;    // sub-block, first 16-byte chunk
+      if (BN == 16) {
+        ldsm_x4(sa + q * BN * 128 + arow * 128 + (((c16 + achunk) ^ (arow & 7)) << 4),
+                af[0], af[1], af[2], af[3]);
+      } else {
+        ldsm_x2(sa + q * BN * 128 + arow * 128 + (((c16 + achunk) ^ (arow & 7)) << 4),
+                af[0], af[2]);
+        af[1] = af[3] = 0u;
+      }
+      if (wd)
+        ldsm_x2(sx + q * 1024 + xrow * 128 + (((c16 + xchunk) ^ xrow) << 4), bf[0], bf[1]);
+      else
+        ldsm_x2(sx + xrow * kRowBytes + kk * 32 + xchunk * 16, bf[0], bf[1]);
+    };
+    if (kl == kShrinkKB) {
+      // full k-block: this warp's 16 / W steps, all operands first, then the
+      // MMAs in step order (the same sequence as the loop below)
+      constexpr int NS = 16 / G::WARPS;
+      uint32_t af[NS][4], bf[NS][2];
+#pragma unroll
+      for (int i = 0; i < NS; ++i) frag(warp + i * G::WARPS, af[i], bf[i]);
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        mma_16816(d, af[i][0], af[i][1], af[i][2], af[i][3], bf[i][0], bf[i][1]);
+    } else {
+      for (int kk = warp; kk < n16; kk += G::WARPS) {
+        uint32_t af[4], bf[2];
+        frag(kk, af, bf);
+        mma_16816(d, af[0], af[1], af[2], af[3], bf[0], bf[1]);
+      }
+    }
+    if ((kl & 15) && warp == n16 % G::WARPS) {
+      // the last 8 elements of the partition
+      const int q = n16 >> 2, c = (n16 & 3) * 2;
+      uint32_t a0, a1, b0;
+      if (BN == 16) {
+        ldsm_x2(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0, a1);
+      } else {
+        ldsm_x1(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0);
+        a1 = 0u;
+      }
+      if (wd)
+        ldsm_x1(sx + q * 1024 + xrow * 128 + ((c ^ xrow) << 4), b0);
+      else
+        ldsm_x1(sx + xrow * kRowBytes + n16 * 32, b0);
+      mma_1688(d, a0, a1, b0);
+    }
+  }
 
+  // Warp sums -> shared memory (stage 0: no copy in flight and every warp
+  // done reading the stages), then thread o adds the W values of output o in
+  // warp order.
+  __device__ __forceinline__ void reduce_warps(const float (&d)[4], float& out) const {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* red = reinterpret_cast<float*>(stages);
+    const int g = lane >> 2, t = lane & 3;
+    red[warp * G::TB + (2 * t) * BN + g] = d[0];
+    red[warp * G::TB + (2 * t + 1) * BN + g] = d[1];
+    if (BN == 16) {
+      red[warp * G::TB + (2 * t) * BN + g + 8] = d[2];
+      red[warp * G::TB + (2 * t + 1) * BN + g + 8] = d[3];
+    }
+    __syncthreads();
+    float v = red[tid];
+#pragma unroll
+    for (int w = 1; w < G::WARPS; ++w) v += red[w * G::TB + tid];
+    out = v;
+  }
+
+  // All threads. The first min(nkb, nst) k-blocks must already be armed and
+  // issued. On return `out` is this thread's output:
+  // token row tid / BN, rank tid % BN (not yet scaled). Returns false if a
+  // copy wait expired (after draining, bounded, every copy still in flight).
+  __device__ __forceinline__ bool run(const PartialArgs& a, float& out) const {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int issued = min(nkb, nst);
     int fail_b = -1;
     for (int b = 0; b < nkb; ++b) {
@@ -160,59 +239,7 @@ struct PartialRing {
       const uint32_t parity = (uint32_t)((b / nst) & 1);
       const bool ok = mbar_wait_bounded(&bars[st], parity, a.status);
       if (__syncthreads_or(!ok)) { fail_b = b; break; }
-      const int kl = klen(a, b);
-      const int n16 = kl / 16;
-      const uint32_t sx = smem_u32(stages + st * kStageBytes);
-      const uint32_t sa = sx + kXBytes;
-      // operands of step kk (16 elements): A fragment (ranks) and x fragment (tokens)
-      auto frag = [&](int kk, uint32_t (&af)[4], uint32_t (&bf)[2]) {
-        const int q = kk >> 2, c16 = (kk & 3) * 2;    // sub-block, first 16-byte chunk
-        if (BN == 16) {
-          ldsm_x4(sa + q * BN * 128 + arow * 128 + (((c16 + achunk) ^ (arow & 7)) << 4),
-                  af[0], af[1], af[2], af[3]);
-        } else {
-          ldsm_x2(sa + q * BN * 128 + arow * 128 + (((c16 + achunk) ^ (arow & 7)) << 4),
-                  af[0], af[2]);
-          af[1] = af[3] = 0u;
-        }
-        if (wd)
-          ldsm_x2(sx + q * 1024 + xrow * 128 + (((c16 + xchunk) ^ xrow) << 4), bf[0], bf[1]);
-        else
-          ldsm_x2(sx + xrow * kRowBytes + kk * 32 + xchunk * 16, bf[0], bf[1]);
-      };
-      if (kl == kShrinkKB) {
-        // full k-block: this warp's 16 / W steps, all operands first, then the
-        // MMAs in step order (the same sequence as the loop below)
-        constexpr int NS = 16 / G::WARPS;
-        uint32_t af[NS][4], bf[NS][2];
-#pragma unroll
-        for (int i = 0; i < NS; ++i) frag(warp + i * G::WARPS, af[i], bf[i]);
-#pragma unroll
-        for (int i = 0; i < NS; ++i)
-          mma_16816(d, af[i][0], af[i][1], af[i][2], af[i][3], bf[i][0], bf[i][1]);
-      } else {
-        for (int kk = warp; kk < n16; kk += G::WARPS) {
-          uint32_t af[4], bf[2];
-          frag(kk, af, bf);
-          mma_16816(d, af[0], af[1], af[2], af[3], bf[0], bf[1]);
-        }
-      }
-      if ((kl & 15) && warp == n16 % G::WARPS) {
-        // the last 8 elements of the partition
-        const int q = n16 >> 2, c = (n16 & 3) * 2;
-        uint32_t a0, a1, b0;
-        if (BN == 16) {
-          ldsm_x2(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0, a1);
-        } else {
-          ldsm_x1(sa + q * BN * 128 + arow * 128 + ((c ^ (arow & 7)) << 4), a0);
-          a1 = 0u;
-        }
-        if (wd)
-          ldsm_x1(sx + q * 1024 + xrow * 128 + ((c ^ xrow) << 4), b0);
-        else
-          ldsm_x1(sx + xrow * kRowBytes + n16 * 32, b0);
-        mma_1688(d, a0, a1, b0);
-      }
+      mma_kblock(a, st, klen(a, b), d);
       __syncthreads();
       if (b + nst < nkb) {
         if (warp == 0) {
@@ -230,22 +257,7 @@ struct PartialRing {
       __syncthreads();
       return false;
     }
-
-    // Warp sums -> shared memory (stage 0, no copy in flight any more), then
-    // thread o adds the W values of output o in warp order.
-    float* red = reinterpret_cast<float*>(stages);
-    const int g = lane >> 2, t = lane & 3;
-    red[warp * G::TB + (2 * t) * BN + g] = d[0];
-    red[warp * G::TB + (2 * t + 1) * BN + g] = d[1];
-    if (BN == 16) {
-      red[warp * G::TB + (2 * t) * BN + g + 8] = d[2];
-      red[warp * G::TB + (2 * t + 1) * BN + g + 8] = d[3];
-    }
-    __syncthreads();
-    float v = red[tid];
-#pragma unroll
-    for (int w = 1; w < G::WARPS; ++w) v += red[w * G::TB + tid];
-    out = v;
+    reduce_warps(d, out);
     return true;
   }
 };

@@ -22,7 +22,8 @@
 // Latency: the tile entry is read before griddep_wait() (the token map is
 // complete before this kernel starts); with IG_FLAG_STATIC_WEIGHTS the A
 // rows of the first stages are requested before it too, so only the x rows
-// wait for the previous kernel.
+// wait for the previous kernel; L2 is asked for those early as well, and the
+// first k-blocks' x copies are issued by different warps.
 //
 // Reduction order inside a partition (shrink_core.cuh): 16-element steps
 // dealt round-robin to the warps, each warp's steps accumulated in increasing
@@ -117,7 +118,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   pa.nrows = nrows;
   pa.tm_x = &p.tm_x;
   pa.tm_xs = &p.tm_xs;
-  pa.wide_rows = p.x_wide_rows;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)k0;
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   ring.bars = bars;
   ring.nst = kShrinkStages;
   ring.nkb = (int)((p.Ks + kShrinkKB - 1) / kShrinkKB);
+  pa.wide_rows = p.x_wide_rows;
 
   const int first = min(ring.nkb, kShrinkStages);
   if (warp == 0) {
@@ -134,16 +135,16 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
       ring.expect(pa, b);
       if (early_a) ring.issue_a(pa, b);
     }
+  } else if (warp == 1 && (threadIdx.x & 31) < nrows) {
+    // L2 prefetch of the x rows (no effect on the values read after the wait)
+    bulk_prefetch_l2(p.x + (int64_t)rows_s[threadIdx.x & 31] * p.K + k0, (uint32_t)(p.Ks * 2));
   }
   griddep_wait();
   griddep_launch();
-  if (warp == 0) {
-    for (int b = 0; b < first; ++b) {
-      if (!early_a) ring.issue_a(pa, b);
-      ring.issue_x(pa, b);
-    }
-  }
-
+  if (warp == 0 && !early_a)
+    for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
+  // one k-block per warp, so that the copies leave the warps in parallel
+  for (int b = warp; b < first; b += ShrinkGeo<BN>::WARPS) ring.issue_x(pa, b);
   float v;
   const bool ok = ring.run(pa, v);
   if (CL) {
