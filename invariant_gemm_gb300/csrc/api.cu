@@ -261,23 +261,21 @@ int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const voi
   if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st);
   ShrinkParams p;
   const bool fma = pl.path == IG_PATH_FMA;
-  // x: 256-element rows, no swizzle (both paths); A: warp path 64-element
-  // boxes, 128-byte swizzle (ldmatrix operands), FMA path 256, no swizzle
+  // x (FMA path only; the warp path loads x into registers): 256-element
+  // rows, no swizzle; A: warp path 64-element boxes, 128-byte swizzle, FMA
+  // path 256, no swizzle
   const uint32_t kbox = fma ? kShrinkKB : 64;
   const int swz = fma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (rc != IG_OK) return rc;
-  if (!fma) {
-    rc = encode_map_2d(&p.tm_xs, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
-                       1, CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = IG_OK;
+  if (fma) {
+    rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
+                       kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != IG_OK) return rc;
   }
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)pl.bn, swz);
   if (rc != IG_OK) return rc;
   p.has_a3 = !fma && sh->K % 64 == 0 && pl.Ks % 64 == 0;
-  p.x_wide_rows = sh->M >= kXWideMinM ? kTileRows : kTileRows + 1;
   if (p.has_a3) {
     rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                        (uint64_t)sh->K, (uint32_t)pl.bn);
@@ -308,22 +306,20 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
               float scale, float* z, void* y, uint8_t* ws, cudaStream_t st) {
   FusedParams p;
   const bool fma = pl.path == IG_PATH_FMA;
-  // x rows are gathered 4 at a time (box 256 x 1); A blocks are r rows high
+  // FMA path: x rows gathered 4 at a time (box 256 x 1; the warp path loads
+  // x into registers); A blocks are r rows high
   const uint32_t kbox = fma ? kShrinkKB : 64;
   const int swz = fma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
-                         kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (rc != IG_OK) return rc;
-  if (!fma) {
-    rc = encode_map_2d(&p.tm_xs, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
-                       1, CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = IG_OK;
+  if (fma) {
+    rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2,
+                       kShrinkKB, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != IG_OK) return rc;
   }
   rc = encode_map_2d(&p.tm_a, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                      (uint64_t)sh->K, (uint64_t)sh->K * 2, kbox, (uint32_t)sh->r, swz);
   if (rc != IG_OK) return rc;
   p.has_a3 = !fma && sh->K % 64 == 0 && pl.Ks % 64 == 0;
-  p.x_wide_rows = sh->M >= kXWideMinM ? kTileRows : kTileRows + 1;
   if (p.has_a3) {
     rc = encode_map_a3(&p.tm_a3, A, (uint64_t)sh->num_adapters * sh->slices * sh->r,
                        (uint64_t)sh->K, (uint32_t)sh->r);

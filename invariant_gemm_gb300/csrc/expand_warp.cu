@@ -19,9 +19,10 @@
 // the token map's tile table) x 256 output columns of one slice. The
 // block's B columns are copied by TMA as 128-byte rows (128-byte swizzle);
 // the tile's Z rows are read from global memory once, rounded (or split
-// into three bf16 parts with IG_FLAG_Z_FP32) into shared memory. Warp w
-// takes the 8-column blocks w, w+4, ...; lane 4g + t updates row g, columns
-// 2t and 2t+1 of each.
+// into three bf16 parts with IG_FLAG_Z_FP32) into shared memory. The
+// block's columns form 8 groups of 32: warp w takes the groups w and w + 4,
+// and lane 4g + t updates row g, columns 8t .. 8t+7 of each, with one
+// 16-byte load and one 16-byte store of y per group.
 //
 // Latency: the tile entry is read before griddep_wait(); with
 // IG_FLAG_STATIC_WEIGHTS the block's B copy is issued before it too. After
@@ -36,7 +37,7 @@ namespace {
 
 constexpr int kThreads = kExpandWarps * 32;
 constexpr int kMaxRank = 256;
-constexpr int kPre = kExpandBN / 8 / kExpandWarps;   // y words per lane (8)
+constexpr int kGW = kExpandBN / 32 / kExpandWarps;   // 32-column groups per warp (2)
 
 struct ExpandLayout {
   int box_rows, nbox;
@@ -82,7 +83,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t N = p.N;
   const int64_t n0 = (int64_t)nt * kExpandBN;
   const int ncols = (int)min((int64_t)kExpandBN, N - n0);
-  const int nblk = ncols / 8;
   const int brows = ncols * r / 64;
   const int nbox = (brows + lay.box_rows - 1) / lay.box_rows;
   const bool early_b = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
@@ -110,12 +110,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int gq = lane >> 2, tq = lane & 3;
   const bool has_row = gq < nrows;
   __nv_bfloat16* yrow = p.y + (int64_t)ent[4 + min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
-                        (int64_t)sl * N + n0 + 2 * tq;
-  uint32_t ypre[kPre];
+                        (int64_t)sl * N + n0 + 8 * tq;
+  auto y_ok = [&](int cb) { return has_row && cb + 8 * tq < ncols; };
+  uint4 ypre[kGW];
 #pragma unroll
-  for (int i = 0; i < kPre; ++i)
-    if (has_row && warp + i * kExpandWarps < nblk)
-      ypre[i] = *reinterpret_cast<const uint32_t*>(yrow + (warp + i * kExpandWarps) * 8);
+  for (int i = 0; i < kGW; ++i) {
+    const int cb = 32 * (warp + i * kExpandWarps);
+    ypre[i] = y_ok(cb) ? __ldcg(reinterpret_cast<const uint4*>(yrow + cb))
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
 
   // The tile's Z rows -> bf16 parts in shared memory (rows past nrows zero).
   // L2 only: Z was written by the previous kernel.
@@ -136,40 +139,39 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const uint32_t sB_addr = smem_u32(sB);
   const int parts = zf32 ? 3 : 1;
-  auto store = [&](int blk, uint32_t yv, const float (&d)[4]) {
-    if (has_row)
-      *reinterpret_cast<uint32_t*>(yrow + blk * 8) =
-          f32_to_bf16_bits(bf16lo(yv) + d[0]) | (f32_to_bf16_bits(bf16hi(yv) + d[1]) << 16);
+  const int cmax = ncols - 1;
+  auto store = [&](int cb, const uint4& yv, const float (&v)[8]) {
+    if (y_ok(cb)) *reinterpret_cast<uint4*>(yrow + cb) = y_add8(yv, v);
   };
   if (!zf32 && (r == 16 || r == 8)) {
-    // B operands of the warp's blocks, then their MMAs, then the y updates
-    // (the same MMA per block as expand_block_mma)
+    // B operands of the warp's groups, then their MMAs, then the y updates
+    // (the same MMAs as expand_group_mma)
     auto run = [&](auto rank) {
       constexpr int R = decltype(rank)::value;
       ExpandFrag<R> zf;
       zf.load_z(zb, lane);
-      uint32_t bq[kPre][2];
+      uint32_t bq[kGW][4][2];
 #pragma unroll
-      for (int i = 0; i < kPre; ++i)
-        ExpandFrag<R>::load_b(sB_addr, min(warp + i * kExpandWarps, nblk - 1) * 8, lane, bq[i]);
-      float dq[kPre][4];
+      for (int i = 0; i < kGW; ++i)
+        ExpandFrag<R>::load_b(sB_addr, min(32 * (warp + i * kExpandWarps), cmax), cmax, lane,
+                              bq[i]);
+      float v[kGW][8];
 #pragma unroll
-      for (int i = 0; i < kPre; ++i) zf.mma(dq[i], bq[i]);
+      for (int i = 0; i < kGW; ++i) zf.mma(v[i], bq[i]);
 #pragma unroll
-      for (int i = 0; i < kPre; ++i)
-        if (warp + i * kExpandWarps < nblk) store(warp + i * kExpandWarps, ypre[i], dq[i]);
+      for (int i = 0; i < kGW; ++i) store(32 * (warp + i * kExpandWarps), ypre[i], v[i]);
     };
     if (r == 16) run(std::integral_constant<int, 16>());
     else run(std::integral_constant<int, 8>());
     return;
   }
 #pragma unroll
-  for (int i = 0; i < kPre; ++i) {
-    const int blk = warp + i * kExpandWarps;
-    if (blk >= nblk) break;
-    float d[4];
-    expand_block_mma(d, sB_addr, blk * 8, r, zb, parts, lane);
-    store(blk, ypre[i], d);
+  for (int i = 0; i < kGW; ++i) {
+    const int cb = 32 * (warp + i * kExpandWarps);
+    if (cb >= ncols) break;
+    float v[8];
+    expand_group_mma(v, sB_addr, cb, cmax, r, zb, parts, lane);
+    store(cb, ypre[i], v);
   }
 }
 

@@ -21,22 +21,18 @@
 // Bit-for-bit the same results as the two-kernel path (shrink kernel with
 // the counter protocol, then the expand kernel): the partials come from the
 // same code (shrink_core.cuh), the combine adds them in the same order, and
-// the expand keeps the same j order and single rounding.
+// the expand keeps the same j order and single rounding (warp_mma.cuh).
 //
 // Block = r/4 warps; cluster = S blocks (rank s = K partition s); tile = up
 // to 8 token rows of one adapter (tile-table entry) x all r rank columns
-// (r = 8 or 16). Copies: per 64-element sub-block the A rows by one tiled TMA
-// copy and the token rows of x by row-gather TMA copies (4 rows each), the
-// first k-blocks issued by different warps (a TMA copy issued after
-// griddepcontrol.wait took a few hundred ns to leave its warp on GB300, so
-// one warp issuing them all serialised them); the block's B column slice by
-// tiled TMA copies of 128-byte rows (64/r columns x r ranks each); all
-// 128-byte swizzled, so that ldmatrix reads of 8 rows hit 8 distinct bank
-// groups. Before griddep_wait, L2 is asked for the block's x and y rows
-// (0.3 us per layer at 256 tokens). The y values a lane will update are
-// loaded into registers right after the x copies are issued, so they arrive
-// while the shrink computes. Both the shrink partial and the expand run on
-// the warp-level tensor cores (warp_mma.cuh).
+// (r = 8 or 16). Copies: the A rows of the partition by TMA (128-byte
+// swizzled, one 3-D copy per 256 elements), and the block's B column slice
+// by tiled TMA copies of 128-byte rows (64/r columns x r ranks each), both
+// issued before griddep_wait when the weights are static; x and y go
+// straight from global memory into registers in 16-byte loads right after
+// the wait (L2 was asked for the block's x and y rows before it), so that y
+// arrives while the shrink computes. Both the shrink partial and the expand
+// run on the warp-level tensor cores.
 #include "shrink_core.cuh"
 
 namespace ig {
@@ -55,7 +51,7 @@ struct FusedLayout {
   int cols;          // output columns per block (multiple of 8)
   int box_rows;      // B rows (128 bytes) per TMA box (<= 256)
   int nbox;          // B boxes per block
-  size_t ring_off, part_off, zb_off, b_off, bytes;   // from the 1024-aligned base
+  size_t ring_off, part_off, red_off, zb_off, b_off, bytes;   // from the 1024-aligned base
 };
 
 template <int BN>
@@ -70,20 +66,24 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   L.nbox = (brows + L.box_rows - 1) / L.box_rows;
   L.ring_off = 1024;
   L.part_off = L.ring_off + (size_t)L.nst * PartialRing<BN>::kStageBytes;
-  L.zb_off = L.part_off + (size_t)S * F::TB * 4;
+  L.red_off = L.part_off + (size_t)S * F::TB * 4;
+  L.zb_off = L.red_off + PartialRing<BN>::kRedBytes;
   L.b_off = (L.zb_off + (size_t)3 * F::TB * 2 + 1023) / 1024 * 1024;
   L.bytes = L.b_off + (size_t)L.nbox * L.box_rows * 128;
   return L;
 }
 
+// At most 128 registers a thread for BN = 16 (four blocks of 128 threads
+// per SM), so that the next layer's blocks fit beside this layer's and run
+// their prologue early.
 template <int BN>
-__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
+__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::THREADS)
     fused_warp_kernel(const __grid_constant__ FusedParams p) {
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
   constexpr int W = ShrinkGeo<BN>::WARPS;
   constexpr int TB = FusedGeo<BN>::TB;
   constexpr int CU = FusedGeo<BN>::CU;
-  constexpr int kPre = 64 / W;   // y words prefetched per lane: 512 columns per block
+  constexpr int kGB = 4;   // 32-column groups per warp whose y is loaded together
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   uint64_t* bar_part = bars + kShrinkStages + 1;                 // incoming partials
   int32_t* ent_s = reinterpret_cast<int32_t*>(smem + 64);        // tile entry
   float* part = reinterpret_cast<float*>(smem + lay.part_off);   // [S][8][BN]
+  float* red = reinterpret_cast<float*>(smem + lay.red_off);     // warp sums
   uint16_t* zb = reinterpret_cast<uint16_t*>(smem + lay.zb_off); // [3][8][BN] bf16 parts of Z
   uint8_t* sB = smem + lay.b_off;                                // 128-byte rows, swizzled
 
@@ -105,7 +106,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
 
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
   if (tid == 0) {
-    prefetch_tensormap(&p.tm_x);
     prefetch_tensormap(p.has_a3 ? &p.tm_a3 : &p.tm_a);
     prefetch_tensormap(&p.tm_b);
     for (int i = 0; i < lay.nst; ++i) mbar_init(&bars[i], 1);
@@ -138,16 +138,15 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   // this block's output columns [c0, c0 + ncols) of slice sl
   const int64_t c0 = (int64_t)s * lay.cols;
   const int ncols = (int)max((int64_t)0, min((int64_t)lay.cols, N - c0));
-  const int nblk = ncols / 8;
   const bool early_w = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
 
   PartialArgs pa;
   pa.rows = rows_s;
   pa.status = p.status;
+  pa.x = p.x;
+  pa.K = p.K;
   pa.Ks = p.Ks;
   pa.nrows = nrows;
-  pa.tm_x = &p.tm_x;
-  pa.tm_xs = &p.tm_xs;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)((int64_t)s * p.Ks);
@@ -158,7 +157,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   ring.nst = lay.nst;
   ring.nkb = (int)((p.Ks + kShrinkKB - 1) / kShrinkKB);
   const int first = min(ring.nkb, lay.nst);
-  pa.wide_rows = p.x_wide_rows;
 
   // B rows of this block: 128-byte row u holds columns c0 + CU*u .. + CU-1
   const int b_row0 = (int)((((int64_t)g * p.slices + sl) * N + c0) / CU);
@@ -189,33 +187,43 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
                            (int64_t)sl * N + c0,
                        (uint32_t)(ncols * 2));
   }
+  // Everything that depends only on the token map is computed before the
+  // wait: this lane's x row, and the expand geometry. The block's columns
+  // form groups of 32 (the last one may be partial); warp w takes the groups
+  // w, w + W, ...; lane 4g + t updates row g, columns 8t .. 8t+7 of each
+  // (warp_mma.cuh). The y of its first kGB groups is loaded right after the
+  // x loads and arrives during the shrink.
+  const __nv_bfloat16* xrow = ring.x_row(pa);
+  const int gq = lane >> 2, tq = lane & 3;
+  const bool has_row = gq < nrows;
+  __nv_bfloat16* yrow = p.y + (int64_t)rows_s[min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
+                        (int64_t)sl * N + c0 + 8 * tq;
+  const int ngroups = (ncols + 31) / 32;
+  auto y_ok = [&](int grp) { return has_row && grp < ngroups && 32 * grp + 8 * tq < ncols; };
+  auto load_y = [&](int h, uint4 (&yq)[kGB]) {
+#pragma unroll
+    for (int i = 0; i < kGB; ++i) {
+      const int grp = warp + (h + i) * W;
+      yq[i] = y_ok(grp) ? __ldcg(reinterpret_cast<const uint4*>(yrow + 32 * grp))
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  // Static weights and a short partition: this lane's A chunks go into
+  // registers now, while the previous kernel still runs.
+  const bool fast = ring.fast(early_w);
+  typename PartialRing<BN>::ARegs ar[PartialRing<BN>::kFastKB];
+  const bool a_ok = fast ? ring.fast_prologue(pa, ar) : true;
+
   griddep_wait();
   griddep_launch();
   if (warp == 0 && !early_w) {
     for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
     issue_b();
   }
-  // Expand geometry: warp w takes the 8-column blocks w, w + W, ...; lane
-  // 4g + t updates row g, columns 2t and 2t+1 of each (one bf16 pair of y).
-  // Its first kPre pairs are loaded right after the x copies are issued and
-  // arrive during the shrink.
-  const int gq = lane >> 2, tq = lane & 3;
-  const bool has_row = gq < nrows;
-  __nv_bfloat16* yrow = p.y + (int64_t)rows_s[min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
-                        (int64_t)sl * N + c0 + 2 * tq;
-  uint32_t ypre[kPre];
-  auto load_ypre = [&]() {
-#pragma unroll
-    for (int i = 0; i < kPre; ++i)
-      if (has_row && warp + i * W < nblk)
-        ypre[i] = *reinterpret_cast<const uint32_t*>(yrow + (warp + i * W) * 8);
-  };
-  // one k-block per warp, so that the copies leave the warps in parallel
-  for (int b = warp; b < first; b += W) ring.issue_x(pa, b);
-  load_ypre();
-
+  uint4 ypre[kGB];
   float v;
-  const bool ok = ring.run(pa, v);
+  const bool ok = fast ? ring.fast_run(pa, xrow, ar, a_ok, red, v, [&]() { load_y(0, ypre); })
+                       : ring.run(pa, xrow, red, v, [&]() { load_y(0, ypre); });
 
   // Send this block's partial P_s to slot s of every block of the cluster
   // (its own included). Every block sends on every path (zeros after a
@@ -227,13 +235,25 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
       st_async_f32(map_rank(part + s * TB + tid, (uint32_t)q), pv,
                    map_rank(bar_part, (uint32_t)q));
   }
+  // While the partials travel: the B operands of this warp's first kGB
+  // column groups (one Z part), from the slice that landed during the shrink.
+  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
+  const bool copies_ok = mbar_wait_bounded(bar_b, 0, p.status);
+  const uint32_t sB_addr = smem_u32(sB);
+  const int cmax = ncols - 1;
+  uint32_t bq[kGB][4][2];
+  auto load_bq = [&](int h) {
+#pragma unroll
+    for (int i = 0; i < kGB; ++i)
+      ExpandFrag<BN>::load_b(sB_addr, 32 * (warp + (h + i) * W), cmax, lane, bq[i]);
+  };
+  if (copies_ok && !zf32 && warp < ngroups) load_bq(0);
   // The wait outlasts any sender's own bounded waits, so a block never
   // leaves while a partial is still on its way to it.
   const bool got = mbar_wait_bounded(bar_part, 0, p.status, 1ll << 36);
 
   // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
   // Thread o owns output o (token row o / r, rank o % r).
-  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
   {
     const int o = tid;
     uint16_t hi = 0, mid = 0, lo = 0;
@@ -251,77 +271,30 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   __syncthreads();   // zb complete
 
   // Expand this block's columns: y = bf16_rn(f32(y) + D), D the tensor-core
-  // sum over j of bf16(z_j) B_nj (warp_mma.cuh, the same routine as the
-  // two-kernel expand). Every element is computed by one MMA of one warp, so
-  // the split over warps and blocks does not change any result.
-  const bool copies_ok = mbar_wait_bounded(bar_b, 0, p.status);
+  // sum over j of bf16(z_j) B_nj (the same MMAs as the two-kernel expand).
+  // Every element is computed by one MMA of one warp, so the split over
+  // warps and blocks does not change any result. Batches of kGB of the
+  // warp's groups (B operands of the first batch loaded above); the y of the
+  // next batch is loaded before the current one is computed.
   if (copies_ok && got) {
-    const uint32_t sB_addr = smem_u32(sB);
-    const int parts = zf32 ? 3 : 1;
-    auto store = [&](int blk, uint32_t yv, const float (&d)[4]) {
-      if (has_row)
-        *reinterpret_cast<uint32_t*>(yrow + blk * 8) =
-            f32_to_bf16_bits(bf16lo(yv) + d[0]) | (f32_to_bf16_bits(bf16hi(yv) + d[1]) << 16);
-    };
-    if (!zf32) {
-      // Batches of 8 of the warp's blocks: B operands of all 8, then their
-      // MMAs, then the y updates (the MMA of each block is the one
-      // expand_block_mma issues). The first kPre blocks use the prefetched
-      // y; later batches load the y of the next batch before computing the
-      // current one.
-      ExpandFrag<BN> zf;
-      zf.load_z(zb, lane);
-      auto batch = [&](int h, const uint32_t (&yq)[8]) {
-        uint32_t bq[8][2];
+    ExpandFrag<BN> zf;
+    zf.load_z(zb, lane);
+    for (int h = 0; warp + h * W < ngroups; h += kGB) {
+      uint4 ynext[kGB];
+      const bool more = warp + (h + kGB) * W < ngroups;
+      if (more) load_y(h + kGB, ynext);
+      if (h > 0 && !zf32) load_bq(h);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          ExpandFrag<BN>::load_b(sB_addr, min(warp + (h + i) * W, nblk - 1) * 8, lane, bq[i]);
-        float dq[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) zf.mma(dq[i], bq[i]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (warp + (h + i) * W < nblk) store(warp + (h + i) * W, yq[i], dq[i]);
-      };
-      auto load_y = [&](int h, uint32_t (&yq)[8]) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int blk = warp + (h + i) * W;
-          yq[i] = (has_row && blk < nblk) ? *reinterpret_cast<const uint32_t*>(yrow + blk * 8)
-                                          : 0u;
-        }
-      };
-      uint32_t ynext[8];
-      if (warp + kPre * W < nblk) load_y(kPre, ynext);
-#pragma unroll
-      for (int h = 0; h < kPre; h += 8) {
-        if (warp + h * W >= nblk) break;
-        uint32_t yq[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) yq[i] = ypre[h + i];
-        batch(h, yq);
+      for (int i = 0; i < kGB; ++i) {
+        const int grp = warp + (h + i) * W;
+        float vv[8];
+        if (!zf32) zf.mma(vv, bq[i]);
+        else expand_group_mma(vv, sB_addr, 32 * grp, cmax, BN, zb, 3, lane);
+        if (y_ok(grp)) *reinterpret_cast<uint4*>(yrow + 32 * grp) = y_add8(ypre[i], vv);
       }
-      for (int h = kPre; warp + h * W < nblk; h += 8) {
-        uint32_t yq[8];
+      if (more) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) yq[i] = ynext[i];
-        if (warp + (h + 8) * W < nblk) load_y(h + 8, ynext);
-        batch(h, yq);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kPre; ++i) {
-        const int blk = warp + i * W;
-        if (blk >= nblk) break;
-        float d[4];
-        expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
-        store(blk, ypre[i], d);
-      }
-      // blocks past the prefetched ones (more than kPre per warp)
-      for (int blk = warp + kPre * W; blk < nblk; blk += W) {
-        float d[4];
-        expand_block_mma(d, sB_addr, blk * 8, BN, zb, parts, lane);
-        store(blk, has_row ? *reinterpret_cast<const uint32_t*>(yrow + blk * 8) : 0u, d);
+        for (int i = 0; i < kGB; ++i) ypre[i] = ynext[i];
       }
     }
   }

@@ -49,12 +49,9 @@ constexpr int kTileInts = 4 + kTileRows;  // [g, nrows, consecutive, 0, rows[8]]
 constexpr int kShrinkKB = 256;        // elements per k-block (4 swizzled sub-blocks of 64)
 constexpr int kShrinkStages = 4;
 constexpr int kExpandWarps = 4;
-constexpr int kExpandBN = 256;        // output columns per expand block: 4 warps x 8 blocks of 8
-// Small-rank path: full tiles take x swizzled from this batch size on (a
-// copy layout only: results do not depend on it).
-constexpr int64_t kXWideMinM = 128;
+constexpr int kExpandBN = 256;        // output columns per expand block: 4 warps x 2 groups of 32
 // Revision of the arithmetic of the kernels; part of the determinism key.
-constexpr int kArithRevision = 3;
+constexpr int kArithRevision = 4;
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
@@ -82,8 +79,7 @@ struct MapParams {
 };
 
 struct ShrinkParams {
-  CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (row gathers)
-  CUtensorMap tm_xs;    // x [M][K], box 64 x 1, 128-byte swizzle (full tiles)
+  CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (FMA path row gathers)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x BN, 128-byte swizzle
   CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, BN, 4} (when has_a3)
   const __nv_bfloat16* x;
@@ -96,7 +92,6 @@ struct ShrinkParams {
   int64_t M, K, r, Ks;
   int32_t slices, L, S, jblocks, flags;
   int32_t has_a3;       // K and K/S multiples of 64: one 3-D copy per k-block of A
-  int32_t x_wide_rows;  // tiles of this many tokens or more take x swizzled
   float scale;
 };
 
@@ -124,8 +119,7 @@ int encode_map_a3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
                   uint32_t box_rows);
 
 struct FusedParams {
-  CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (row gathers)
-  CUtensorMap tm_xs;    // x [M][K], box 64 x 1, 128-byte swizzle (full tiles)
+  CUtensorMap tm_x;     // x [M][K], box 256 x 1, no swizzle (FMA path row gathers)
   CUtensorMap tm_a;     // A_stack as [L*slices*r][K], box 64 x r, 128-byte swizzle
   CUtensorMap tm_a3;    // the same as {64, rows, K/64}, box {64, r, 4} (when has_a3)
   CUtensorMap tm_b;     // B_stack as rows of 64 elements (64/r output columns
@@ -141,7 +135,6 @@ struct FusedParams {
   int32_t slices, L, S, flags;
   int32_t b_box_rows;
   int32_t has_a3;
-  int32_t x_wide_rows;  // tiles of this many tokens or more take x swizzled
   float scale;
 };
 
@@ -239,10 +232,23 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
 }
 
-// FP32 -> BF16, round to nearest, ties to even (cvt.rn.bf16.f32).
+// FP32 -> BF16 bits, round to nearest, ties to even, on the integer
+// pipes (the conversion unit's cvt costs a long-latency instruction per
+// value, and the expand converts 8 values per lane and column group). RNE of
+// the 16 bits that are dropped: add 0x7FFF plus the lowest kept bit, keep the
+// high half. A carry out of the mantissa steps the exponent up, through to
+// infinity, as rounding must; subnormals round the same way (bf16 and FP32
+// share the exponent range). NaN gives the quiet NaN 0x7FFF.
+__device__ __forceinline__ uint32_t bf16_rne_hi(uint32_t u) {   // rounded value in bits 16..31
+  const uint32_t r = u + 0x7FFFu + ((u >> 16) & 1u);
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FFF0000u : r;
+}
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
-  __nv_bfloat16 h = __float2bfloat16_rn(f);
-  return (uint32_t)__bfloat16_as_ushort(h);
+  return bf16_rne_hi(__float_as_uint(f)) >> 16;
+}
+// Two values: lo -> bits 0..15, hi -> bits 16..31 (one byte permute).
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
+  return __byte_perm(bf16_rne_hi(__float_as_uint(lo)), bf16_rne_hi(__float_as_uint(hi)), 0x7632);
 }
 __device__ __forceinline__ float bf16_round_f32(float f) {
   return __uint_as_float(f32_to_bf16_bits(f) << 16);

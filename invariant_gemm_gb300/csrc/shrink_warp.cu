@@ -15,20 +15,20 @@
 //
 // Block = BN/4 warps, tile = up to 8 token rows of one adapter (one entry of
 // the token map's tile table) x BN rank columns, one K partition; thread o
-// ends with the output of token row o / BN, rank o % BN. The partition is
-// streamed through shared memory in k-blocks of 256 elements by TMA copies
-// (completion counted on an mbarrier), four stages deep.
+// ends with the output of token row o / BN, rank o % BN. The A rows of the
+// partition are streamed through shared memory in k-blocks of 256 elements
+// by TMA copies (completion counted on an mbarrier), four stages deep; x goes
+// from global memory straight into registers (shrink_core.cuh).
 //
 // Latency: the tile entry is read before griddep_wait() (the token map is
 // complete before this kernel starts); with IG_FLAG_STATIC_WEIGHTS the A
 // rows of the first stages are requested before it too, so only the x rows
-// wait for the previous kernel; L2 is asked for those early as well, and the
-// first k-blocks' x copies are issued by different warps.
+// wait for the previous kernel; L2 is asked for those early as well.
 //
-// Reduction order inside a partition (shrink_core.cuh): 16-element steps
-// dealt round-robin to the warps, each warp's steps accumulated in increasing
-// k by bf16 MMAs into FP32, then the warp sums added in warp order. It
-// depends only on K/S and BN.
+// Reduction order inside a partition (shrink_core.cuh): 64-element groups
+// dealt round-robin to the warps, each warp's groups accumulated in
+// increasing k by bf16 MMAs into two FP32 accumulators, then the warp sums
+// added in warp order. It depends only on K/S and BN.
 #include <map>
 #include <mutex>
 
@@ -41,8 +41,9 @@ namespace {
 template <int BN>
 struct ShrinkSmem {
   static constexpr int kStagesOff = 1024;                          // mbarriers + info
+  static constexpr int kRedOff = kStagesOff + kShrinkStages * PartialRing<BN>::kStageBytes;
   // + 1024: the base is aligned to 1024 bytes (128-byte swizzle atoms)
-  static constexpr int kBytes = 1024 + kStagesOff + kShrinkStages * PartialRing<BN>::kStageBytes;
+  static constexpr int kBytes = 1024 + kRedOff + PartialRing<BN>::kRedBytes;
 };
 
 // CL (IG_MODE_DET only): the S partition blocks of a tile form a cluster;
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   float* recv = reinterpret_cast<float*>(smem + 256);        // [S][TB/S] (TB floats)
   constexpr int TB = ShrinkGeo<BN>::TB;
   uint8_t* stages = smem + SM::kStagesOff;
+  float* red = reinterpret_cast<float*>(smem + SM::kRedOff);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int S = p.S;
@@ -116,8 +118,8 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   pa.status = p.status;
   pa.Ks = p.Ks;
   pa.nrows = nrows;
-  pa.tm_x = &p.tm_x;
-  pa.tm_xs = &p.tm_xs;
+  pa.x = p.x;
+  pa.K = p.K;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)k0;
@@ -127,7 +129,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   ring.bars = bars;
   ring.nst = kShrinkStages;
   ring.nkb = (int)((p.Ks + kShrinkKB - 1) / kShrinkKB);
-  pa.wide_rows = p.x_wide_rows;
 
   const int first = min(ring.nkb, kShrinkStages);
   if (warp == 0) {
@@ -139,14 +140,19 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     // L2 prefetch of the x rows (no effect on the values read after the wait)
     bulk_prefetch_l2(p.x + (int64_t)rows_s[threadIdx.x & 31] * p.K + k0, (uint32_t)(p.Ks * 2));
   }
+  // static weights and a short partition: A chunks into registers before
+  // the wait (shrink_core.cuh)
+  const __nv_bfloat16* xrow = ring.x_row(pa);
+  const bool fast = ring.fast(early_a);
+  typename PartialRing<BN>::ARegs ar[PartialRing<BN>::kFastKB];
+  const bool a_ok = fast ? ring.fast_prologue(pa, ar) : true;
   griddep_wait();
   griddep_launch();
   if (warp == 0 && !early_a)
     for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
-  // one k-block per warp, so that the copies leave the warps in parallel
-  for (int b = warp; b < first; b += ShrinkGeo<BN>::WARPS) ring.issue_x(pa, b);
   float v;
-  const bool ok = ring.run(pa, v);
+  const bool ok = fast ? ring.fast_run(pa, xrow, ar, a_ok, red, v, []() {})
+                       : ring.run(pa, xrow, red, v, []() {});
   if (CL) {
     // Send output tid's partial to its owner; every block sends on every
     // path (zeros after a failed copy), so every owner receives TB * 4 bytes.

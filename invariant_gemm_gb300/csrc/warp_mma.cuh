@@ -70,46 +70,65 @@ __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1
 // Round-to-nearest-even bf16 bits of an FP32 value, as the low half.
 __device__ __forceinline__ uint32_t bf16_bits(float f) { return f32_to_bf16_bits(f); }
 
-// One 8-column block of the expand on the tensor cores:
-//   D[m][n] = sum over j of Zb[m][j] * B[cb + n][j],  m < 8 (rows 8..15 zero)
+// The expand on the tensor cores, one group of 32 output columns at a time:
+//   D[m][n] = sum over j of Zb[m][j] * B[n][j],  m < 8 (rows 8..15 zero)
 // j in increasing 16-element chunks (an 8-element chunk last when r % 16 ==
 // 8); with three Z parts (FP32 Z) the hi, mid and lo MMAs of a chunk follow
-// each other. zb: bf16 [parts][8][r] in shared memory; sB: the B columns,
+// each other. A group is 4 MMAs of 8 columns (i = 0..3): column 2t' + e of
+// MMA i is the group's column 8t' + i + 4e, so that lane 4g + t ends with
+// the 8 consecutive columns 8t .. 8t+7 of row g (v[c] holds column 8t + c)
+// and updates them in y with one 16-byte load and one 16-byte store. Which
+// MMA computes a column does not change its value: every element is one
+// MMA's dot product over all of j, in the same order. Under the 128-byte
+// swizzle the 8 column addresses of one ldmatrix fall in 8 distinct bank
+// groups for r = 8 and r = 16.
+// zb: bf16 [parts][8][r] in shared memory; sB: the block's B columns,
 // column c at elements c * r .. c * r + r - 1 of a 128-byte-swizzled buffer
-// (see swz128). Returns d0 = D[g][2t], d1 = D[g][2t+1].
-__device__ __forceinline__ void expand_block_mma(float (&d)[4], uint32_t sB_addr, int cb,
-                                                 int r, const uint16_t* zb, int parts,
-                                                 int lane) {
+// (see swz128); cb: the group's first column; columns past cmax are read as
+// column cmax (their results are not used).
+__device__ __forceinline__ int group_col(int cb, int i, int lane, int cmax) {
+  const int n = lane & 7;   // the MMA column whose B row address this lane gives
+  return min(cb + 8 * (n >> 1) + i + 4 * (n & 1), cmax);
+}
+
+__device__ __forceinline__ void expand_group_mma(float (&v)[8], uint32_t sB_addr, int cb,
+                                                 int cmax, int r, const uint16_t* zb,
+                                                 int parts, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  d[0] = d[1] = d[2] = d[3] = 0.0f;
-  const int c = cb + (lane & 7);              // the column whose row address this lane gives
   const int jsel = ((lane >> 3) & 1) * 8;     // matrix 1: elements 8..15 of the chunk
   const uint32_t* z32 = reinterpret_cast<const uint32_t*>(zb);
   const int zrow = g * (r / 2);               // this lane's Z row, in bf16 pairs
-  int j = 0;
-  for (; j + 16 <= r; j += 16) {
-    uint32_t b0, b1;
-    ldsm_x2(sB_addr + swz128((uint32_t)(c * r + j + jsel)), b0, b1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int c = group_col(cb, i, lane, cmax);
+    int j = 0;
+    for (; j + 16 <= r; j += 16) {
+      uint32_t b0, b1;
+      ldsm_x2(sB_addr + swz128((uint32_t)(c * r + j + jsel)), b0, b1);
 #pragma unroll 1
-    for (int q = 0; q < parts; ++q) {
-      const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
-      mma_16816(d, zp[0], 0u, zp[4], 0u, b0, b1);
+      for (int q = 0; q < parts; ++q) {
+        const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
+        mma_16816(d, zp[0], 0u, zp[4], 0u, b0, b1);
+      }
     }
-  }
-  if (j < r) {   // last 8 elements
-    uint32_t b0;
-    ldsm_x1(sB_addr + swz128((uint32_t)(c * r + j)), b0);
+    if (j < r) {   // last 8 elements
+      uint32_t b0;
+      ldsm_x1(sB_addr + swz128((uint32_t)(c * r + j)), b0);
 #pragma unroll 1
-    for (int q = 0; q < parts; ++q) {
-      const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
-      mma_1688(d, zp[0], 0u, b0);
+      for (int q = 0; q < parts; ++q) {
+        const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
+        mma_1688(d, zp[0], 0u, b0);
+      }
     }
+    v[i] = d[0];
+    v[4 + i] = d[1];
   }
 }
 
-// The same MMA as expand_block_mma for r = R (16 or 8) and one Z part, split
-// into its operand loads so that a warp can issue the loads of many blocks
-// before their MMAs.
+// The same MMAs as expand_group_mma for r = R (16 or 8) and one Z part,
+// split into operand loads and MMAs so that a warp can issue the loads of
+// several groups before their MMAs.
 template <int R>
 struct ExpandFrag {
   uint32_t za0, za2;   // Zb fragment: row g, j 2t..2t+1 and j 2t+8..2t+9 (R = 16)
@@ -119,21 +138,40 @@ struct ExpandFrag {
     za0 = z32[0];
     za2 = R == 16 ? z32[4] : 0u;
   }
-  __device__ __forceinline__ static void load_b(uint32_t sB_addr, int cb, int lane,
-                                                uint32_t (&b)[2]) {
-    const int c = cb + (lane & 7);
-    if (R == 16) {
-      ldsm_x2(sB_addr + swz128((uint32_t)(c * R + ((lane >> 3) & 1) * 8)), b[0], b[1]);
-    } else {
-      ldsm_x1(sB_addr + swz128((uint32_t)(c * R)), b[0]);
-      b[1] = 0u;
+  // B operands of the group's 4 MMAs
+  __device__ __forceinline__ static void load_b(uint32_t sB_addr, int cb, int cmax, int lane,
+                                                uint32_t (&b)[4][2]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = group_col(cb, i, lane, cmax);
+      if (R == 16) {
+        ldsm_x2(sB_addr + swz128((uint32_t)(c * R + ((lane >> 3) & 1) * 8)), b[i][0], b[i][1]);
+      } else {
+        ldsm_x1(sB_addr + swz128((uint32_t)(c * R)), b[i][0]);
+        b[i][1] = 0u;
+      }
     }
   }
-  __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&b)[2]) const {
-    d[0] = d[1] = d[2] = d[3] = 0.0f;
-    if (R == 16) mma_16816(d, za0, 0u, za2, 0u, b[0], b[1]);
-    else mma_1688(d, za0, 0u, b[0]);
+  __device__ __forceinline__ void mma(float (&v)[8], const uint32_t (&b)[4][2]) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (R == 16) mma_16816(d, za0, 0u, za2, 0u, b[i][0], b[i][1]);
+      else mma_1688(d, za0, 0u, b[i][0]);
+      v[i] = d[0];
+      v[4 + i] = d[1];
+    }
   }
 };
+
+// y = bf16_rn(f32(y) + v) for 8 consecutive bf16 values (one rounding each).
+__device__ __forceinline__ uint4 y_add8(const uint4& y, const float (&v)[8]) {
+  uint4 o;
+  o.x = f32x2_to_bf16x2_bits(bf16lo(y.x) + v[0], bf16hi(y.x) + v[1]);
+  o.y = f32x2_to_bf16x2_bits(bf16lo(y.y) + v[2], bf16hi(y.y) + v[3]);
+  o.z = f32x2_to_bf16x2_bits(bf16lo(y.z) + v[4], bf16hi(y.z) + v[5]);
+  o.w = f32x2_to_bf16x2_bits(bf16lo(y.w) + v[6], bf16hi(y.w) + v[7]);
+  return o;
+}
 
 }  // namespace ig
