@@ -116,8 +116,9 @@ typedef enum ig_path {
 
 typedef struct ig_shape {
   int64_t M;            /* tokens: rows of x, z and y; 0 is a valid no-op */
-  int64_t K;            /* hidden size H: reduction length of the shrink */
-  int64_t N;            /* output features per slice (Hout) */
+  int64_t K;            /* hidden size H: reduction length of the shrink
+                           (< 2^31) */
+  int64_t N;            /* output features per slice (Hout, < 2^31) */
   int64_t r;            /* adapter rank */
   int32_t slices;       /* stacked projections that share x, e.g. 3 for QKV */
   int32_t num_adapters; /* L: adapters held in A_stack and B_stack */

@@ -48,7 +48,9 @@ int make_plan(const ig_shape* sh, Plan* pl) {
   if (K % 8 || N % 8 || r % 8) return IG_ERR_SHAPE;
   if (sh->slices < 1 || sh->num_adapters < 1) return IG_ERR_SHAPE;
   const int64_t lim = (int64_t)1 << 40;
-  if (M > (1ll << 31) - 1 || K > lim || N > lim || r > 256) return IG_ERR_UNSUPPORTED;
+  // K and N: 32-bit tensor-map coordinates and column indices in the kernels
+  if (M > (1ll << 31) - 1 || K > (1ll << 31) - 1 || N > (1ll << 31) - 1 || r > 256)
+    return IG_ERR_UNSUPPORTED;
   if (M * K > ((int64_t)1 << 46) || (int64_t)sh->slices * N * r > lim) return IG_ERR_UNSUPPORTED;
   if (sh->num_adapters > kMaxAdapters) return IG_ERR_UNSUPPORTED;
   int S = sh->mode == IG_MODE_UNSPLIT ? 1 : sh->split_k;

@@ -158,14 +158,11 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
     if (m[i] < 0) continue;
     float yf[8];
     unpack8(yv[i], yf);
-    uint32_t o[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) o[c] = f32_to_bf16_bits(yf[c] + acc[i][c]);
     uint4 w;
-    w.x = o[0] | (o[1] << 16);
-    w.y = o[2] | (o[3] << 16);
-    w.z = o[4] | (o[5] << 16);
-    w.w = o[6] | (o[7] << 16);
+    w.x = f32x2_to_bf16x2_bits(yf[0] + acc[i][0], yf[1] + acc[i][1]);
+    w.y = f32x2_to_bf16x2_bits(yf[2] + acc[i][2], yf[3] + acc[i][3]);
+    w.z = f32x2_to_bf16x2_bits(yf[4] + acc[i][4], yf[5] + acc[i][5]);
+    w.w = f32x2_to_bf16x2_bits(yf[6] + acc[i][6], yf[7] + acc[i][7]);
     *reinterpret_cast<uint4*>(p.y + (int64_t)m[i] * ld + (int64_t)sl * N + n) = w;
   }
 }

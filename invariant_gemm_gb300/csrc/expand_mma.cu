@@ -291,13 +291,10 @@ __global__ void __launch_bounds__(kThreads)
           uint4 u = *cp;
           float yf[8];
           unpack8(u, yf);
-          uint32_t o[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = f32_to_bf16_bits(yf[e] + v[8 * q + e]);
-          u.x = o[0] | (o[1] << 16);
-          u.y = o[2] | (o[3] << 16);
-          u.z = o[4] | (o[5] << 16);
-          u.w = o[6] | (o[7] << 16);
+          u.x = f32x2_to_bf16x2_bits(yf[0] + v[8 * q + 0], yf[1] + v[8 * q + 1]);
+          u.y = f32x2_to_bf16x2_bits(yf[2] + v[8 * q + 2], yf[3] + v[8 * q + 3]);
+          u.z = f32x2_to_bf16x2_bits(yf[4] + v[8 * q + 4], yf[5] + v[8 * q + 5]);
+          u.w = f32x2_to_bf16x2_bits(yf[6] + v[8 * q + 6], yf[7] + v[8 * q + 7]);
           *cp = u;
         }
       }

@@ -10,8 +10,8 @@
 //   D = tensor-core sum over j of bf16_rn(z[j]) * B[n][j]   (FP32)
 //   y = bf16_rn(f32(y) + D)
 // with the MMA sequence of warp_mma.cuh: 16-element j chunks in increasing
-// order (m16n8k16, then m16n8k8 for a last 8), D rows = the tile's token
-// rows, D columns = 8 output columns. Every element comes from one MMA of
+// order (m16n8k16, then m16n8k8 for a last 8), D rows = 16 output
+// columns, D columns = the tile's 8 token rows. Every element comes from one MMA of
 // one warp, so the result does not depend on the tiling, on M or on the
 // other rows, and it is the same as the fused decode kernel's.
 //
@@ -21,8 +21,8 @@
 // the tile's Z rows are read from global memory once, rounded (or split
 // into three bf16 parts with IG_FLAG_Z_FP32) into shared memory. The
 // block's columns form 8 groups of 32: warp w takes the groups w and w + 4,
-// and lane 4g + t updates row g, columns 8t .. 8t+7 of each, with one
-// 16-byte load and one 16-byte store of y per group.
+// and lane 4g + t updates columns 4g .. 4g+3 of each in the rows of tokens
+// 2t and 2t + 1, with one 8-byte load and store of y per row and group.
 //
 // Latency: the tile entry is read before griddep_wait(); with
 // IG_FLAG_STATIC_WEIGHTS the block's B copy is issued before it too. After
@@ -52,7 +52,11 @@ __host__ __device__ inline ExpandLayout expand_layout(int r, int64_t N) {
   L.nbox = (brows + L.box_rows - 1) / L.box_rows;
   L.zb_off = 64;
   L.b_off = (L.zb_off + (size_t)3 * kTileRows * r * 2 + 1023) / 1024 * 1024;
-  L.bytes = L.b_off + (size_t)L.nbox * L.box_rows * 128;
+  // room for whole 32-column groups (rows past the block's columns are read
+  // by the MMAs of a partial last group, never used)
+  const int rows_alloc = (cols + 31) / 32 * 32 * r / 64;
+  const int rows_loaded = L.nbox * L.box_rows;
+  L.bytes = L.b_off + (size_t)(rows_loaded > rows_alloc ? rows_loaded : rows_alloc) * 128;
   return L;
 }
 
@@ -107,17 +111,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!early_b) issue_b();
 
   const int64_t M = p.M;
+  // lane 4g + t updates columns 4g .. 4g+3 of each of its groups in the rows
+  // of tokens 2t and 2t + 1 (warp_mma.cuh)
   const int gq = lane >> 2, tq = lane & 3;
-  const bool has_row = gq < nrows;
-  __nv_bfloat16* yrow = p.y + (int64_t)ent[4 + min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
-                        (int64_t)sl * N + n0 + 8 * tq;
-  auto y_ok = [&](int cb) { return has_row && cb + 8 * tq < ncols; };
-  uint4 ypre[kGW];
+  const bool has0 = 2 * tq < nrows, has1 = 2 * tq + 1 < nrows;
+  const int64_t ld = (int64_t)p.slices * N;
+  __nv_bfloat16* yrow0 = p.y + (int64_t)ent[4 + min(2 * tq, nrows - 1)] * ld + (int64_t)sl * N +
+                         n0 + 4 * gq;
+  __nv_bfloat16* yrow1 = p.y + (int64_t)ent[4 + min(2 * tq + 1, nrows - 1)] * ld +
+                         (int64_t)sl * N + n0 + 4 * gq;
+  auto col_ok = [&](int cb) { return cb + 4 * gq < ncols; };
+  uint2 ypre[kGW][2];
 #pragma unroll
   for (int i = 0; i < kGW; ++i) {
     const int cb = 32 * (warp + i * kExpandWarps);
-    ypre[i] = y_ok(cb) ? __ldcg(reinterpret_cast<const uint4*>(yrow + cb))
-                       : make_uint4(0u, 0u, 0u, 0u);
+    ypre[i][0] = has0 && col_ok(cb) ? ldg_cg_v2(yrow0 + cb) : make_uint2(0u, 0u);
+    ypre[i][1] = has1 && col_ok(cb) ? ldg_cg_v2(yrow1 + cb) : make_uint2(0u, 0u);
   }
 
   // The tile's Z rows -> bf16 parts in shared memory (rows past nrows zero).
@@ -140,21 +149,27 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sB_addr = smem_u32(sB);
   const int parts = zf32 ? 3 : 1;
   const int cmax = ncols - 1;
-  auto store = [&](int cb, const uint4& yv, const float (&v)[8]) {
-    if (y_ok(cb)) *reinterpret_cast<uint4*>(yrow + cb) = y_add8(yv, v);
+  auto store = [&](int cb, const uint2 (&yv)[2], const float (&v)[8]) {
+    if (!col_ok(cb)) return;
+    if (has0) *reinterpret_cast<uint2*>(yrow0 + cb) = y_add4(yv[0], v[0], v[1], v[2], v[3]);
+    if (has1) *reinterpret_cast<uint2*>(yrow1 + cb) = y_add4(yv[1], v[4], v[5], v[6], v[7]);
   };
   if (!zf32 && (r == 16 || r == 8)) {
-    // B operands of the warp's groups, then their MMAs, then the y updates
+    // A operands of the warp's groups, then their MMAs, then the y updates
     // (the same MMAs as expand_group_mma)
     auto run = [&](auto rank) {
       constexpr int R = decltype(rank)::value;
       ExpandFrag<R> zf;
       zf.load_z(zb, lane);
-      uint32_t bq[kGW][4][2];
+      uint32_t bq[kGW][2][4];
+      uint32_t off[2];
+      ExpandFrag<R>::lane_offsets(lane, warp & 1, off);
 #pragma unroll
-      for (int i = 0; i < kGW; ++i)
-        ExpandFrag<R>::load_b(sB_addr, min(32 * (warp + i * kExpandWarps), cmax), cmax, lane,
-                              bq[i]);
+      for (int i = 0; i < kGW; ++i) {
+        const int grp = warp + i * kExpandWarps;   // whole warp: groups past ncols skipped
+        if (32 * grp < ncols)
+          ExpandFrag<R>::load_b_at(sB_addr + (uint32_t)(grp >> 1) * (128u * R), off, bq[i]);
+      }
       float v[kGW][8];
 #pragma unroll
       for (int i = 0; i < kGW; ++i) zf.mma(v[i], bq[i]);

@@ -275,8 +275,7 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
         uint32_t* ow = reinterpret_cast<uint32_t*>(&out);
 #pragma unroll
         for (int cp = 0; cp < CP; ++cp)
-          ow[cp] = f32_to_bf16_bits(bf16lo(yw[cp]) + acc[cp].x) |
-                   (f32_to_bf16_bits(bf16hi(yw[cp]) + acc[cp].y) << 16);
+          ow[cp] = f32x2_to_bf16x2_bits(bf16lo(yw[cp]) + acc[cp].x, bf16hi(yw[cp]) + acc[cp].y);
         *reinterpret_cast<YV*>(yp) = out;
       }
     }

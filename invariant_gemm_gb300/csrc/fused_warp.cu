@@ -69,7 +69,11 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   L.red_off = L.part_off + (size_t)S * F::TB * 4;
   L.zb_off = L.red_off + PartialRing<BN>::kRedBytes;
   L.b_off = (L.zb_off + (size_t)3 * F::TB * 2 + 1023) / 1024 * 1024;
-  L.bytes = L.b_off + (size_t)L.nbox * L.box_rows * 128;
+  // room for whole 32-column groups (the rows past the block's columns are
+  // read by the expand's MMAs of a partial last group, never used)
+  const int rows_alloc = (L.cols + 31) / 32 * 32 / F::CU;
+  const int rows_loaded = L.nbox * L.box_rows;
+  L.bytes = L.b_off + (size_t)(rows_loaded > rows_alloc ? rows_loaded : rows_alloc) * 128;
   return L;
 }
 
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
   pa.status = p.status;
   pa.x = p.x;
   pa.K = p.K;
-  pa.Ks = p.Ks;
+  pa.Ks = (int)p.Ks;
   pa.nrows = nrows;
   pa.tm_a = &p.tm_a;
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
@@ -190,22 +194,28 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
   // Everything that depends only on the token map is computed before the
   // wait: this lane's x row, and the expand geometry. The block's columns
   // form groups of 32 (the last one may be partial); warp w takes the groups
-  // w, w + W, ...; lane 4g + t updates row g, columns 8t .. 8t+7 of each
-  // (warp_mma.cuh). The y of its first kGB groups is loaded right after the
-  // x loads and arrives during the shrink.
+  // w, w + W, ...; lane 4g + t updates columns 4g .. 4g+3 of each in the rows
+  // of tokens 2t and 2t + 1 (warp_mma.cuh). The y of its first kGB groups is
+  // loaded right after the x loads and arrives during the shrink.
   const __nv_bfloat16* xrow = ring.x_row(pa);
+  uint32_t boff[2];
+  ExpandFrag<BN>::lane_offsets(lane, warp & 1, boff);
   const int gq = lane >> 2, tq = lane & 3;
-  const bool has_row = gq < nrows;
-  __nv_bfloat16* yrow = p.y + (int64_t)rows_s[min(gq, nrows - 1)] * ((int64_t)p.slices * N) +
-                        (int64_t)sl * N + c0 + 8 * tq;
+  const bool has0 = 2 * tq < nrows, has1 = 2 * tq + 1 < nrows;
+  const int64_t ld = (int64_t)p.slices * N;
+  __nv_bfloat16* yrow0 = p.y + (int64_t)rows_s[min(2 * tq, nrows - 1)] * ld + (int64_t)sl * N +
+                         c0 + 4 * gq;
+  __nv_bfloat16* yrow1 = p.y + (int64_t)rows_s[min(2 * tq + 1, nrows - 1)] * ld +
+                         (int64_t)sl * N + c0 + 4 * gq;
   const int ngroups = (ncols + 31) / 32;
-  auto y_ok = [&](int grp) { return has_row && grp < ngroups && 32 * grp + 8 * tq < ncols; };
-  auto load_y = [&](int h, uint4 (&yq)[kGB]) {
+  auto col_ok = [&](int grp) { return grp < ngroups && 32 * grp + 4 * gq < ncols; };
+  auto load_y = [&](int h, uint2 (&yq)[kGB][2]) {
 #pragma unroll
     for (int i = 0; i < kGB; ++i) {
       const int grp = warp + (h + i) * W;
-      yq[i] = y_ok(grp) ? __ldcg(reinterpret_cast<const uint4*>(yrow + 32 * grp))
-                        : make_uint4(0u, 0u, 0u, 0u);
+      const bool ok = col_ok(grp);
+      yq[i][0] = ok && has0 ? ldg_cg_v2(yrow0 + 32 * grp) : make_uint2(0u, 0u);
+      yq[i][1] = ok && has1 ? ldg_cg_v2(yrow1 + 32 * grp) : make_uint2(0u, 0u);
     }
   };
   // Static weights and a short partition: this lane's A chunks go into
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
     for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
     issue_b();
   }
-  uint4 ypre[kGB];
+  uint2 ypre[kGB][2];
   float v;
   const bool ok = fast ? ring.fast_run(pa, xrow, ar, a_ok, red, v, [&]() { load_y(0, ypre); })
                        : ring.run(pa, xrow, red, v, [&]() { load_y(0, ypre); });
@@ -241,11 +251,17 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
   const bool copies_ok = mbar_wait_bounded(bar_b, 0, p.status);
   const uint32_t sB_addr = smem_u32(sB);
   const int cmax = ncols - 1;
-  uint32_t bq[kGB][4][2];
+  uint32_t bq[kGB][2][4];
+  // group g's B rows start at sB + (g / 2) * 128 * BN; this warp's groups all
+  // have the parity of the warp (W is even)
+  // (only groups that exist: the buffer holds ngroups whole groups)
   auto load_bq = [&](int h) {
 #pragma unroll
-    for (int i = 0; i < kGB; ++i)
-      ExpandFrag<BN>::load_b(sB_addr, 32 * (warp + (h + i) * W), cmax, lane, bq[i]);
+    for (int i = 0; i < kGB; ++i) {
+      const int grp = warp + (h + i) * W;
+      if (grp < ngroups)
+        ExpandFrag<BN>::load_b_at(sB_addr + (uint32_t)(grp >> 1) * (128u * BN), boff, bq[i]);
+    }
   };
   if (copies_ok && !zf32 && warp < ngroups) load_bq(0);
   // The wait outlasts any sender's own bounded waits, so a block never
@@ -280,7 +296,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
     ExpandFrag<BN> zf;
     zf.load_z(zb, lane);
     for (int h = 0; warp + h * W < ngroups; h += kGB) {
-      uint4 ynext[kGB];
+      uint2 ynext[kGB][2];
       const bool more = warp + (h + kGB) * W < ngroups;
       if (more) load_y(h + kGB, ynext);
       if (h > 0 && !zf32) load_bq(h);
@@ -290,11 +306,19 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
         float vv[8];
         if (!zf32) zf.mma(vv, bq[i]);
         else expand_group_mma(vv, sB_addr, 32 * grp, cmax, BN, zb, 3, lane);
-        if (y_ok(grp)) *reinterpret_cast<uint4*>(yrow + 32 * grp) = y_add8(ypre[i], vv);
+        if (col_ok(grp)) {
+          if (has0)
+            *reinterpret_cast<uint2*>(yrow0 + 32 * grp) = y_add4(ypre[i][0], vv[0], vv[1], vv[2], vv[3]);
+          if (has1)
+            *reinterpret_cast<uint2*>(yrow1 + 32 * grp) = y_add4(ypre[i][1], vv[4], vv[5], vv[6], vv[7]);
+        }
       }
       if (more) {
 #pragma unroll
-        for (int i = 0; i < kGB; ++i) ypre[i] = ynext[i];
+        for (int i = 0; i < kGB; ++i) {
+          ypre[i][0] = ynext[i][0];
+          ypre[i][1] = ynext[i][1];
+        }
       }
     }
   }

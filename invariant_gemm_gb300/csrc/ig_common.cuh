@@ -232,23 +232,17 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
 }
 
-// FP32 -> BF16 bits, round to nearest, ties to even, on the integer
-// pipes (the conversion unit's cvt costs a long-latency instruction per
-// value, and the expand converts 8 values per lane and column group). RNE of
-// the 16 bits that are dropped: add 0x7FFF plus the lowest kept bit, keep the
-// high half. A carry out of the mantissa steps the exponent up, through to
-// infinity, as rounding must; subnormals round the same way (bf16 and FP32
-// share the exponent range). NaN gives the quiet NaN 0x7FFF.
-__device__ __forceinline__ uint32_t bf16_rne_hi(uint32_t u) {   // rounded value in bits 16..31
-  const uint32_t r = u + 0x7FFFu + ((u >> 16) & 1u);
-  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FFF0000u : r;
-}
+// FP32 -> BF16 bits, round to nearest, ties to even (cvt.rn.bf16.f32).
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
-  return bf16_rne_hi(__float_as_uint(f)) >> 16;
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
-// Two values: lo -> bits 0..15, hi -> bits 16..31 (one byte permute).
+// Two values in one conversion (cvt.rn.bf16x2.f32): lo -> bits 0..15, hi ->
+// bits 16..31. Where values come in pairs this is the cheapest rounding on
+// GB300: half the conversion instructions of the scalar form, and fewer
+// issue slots than rounding on the integer pipes.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
-  return __byte_perm(bf16_rne_hi(__float_as_uint(lo)), bf16_rne_hi(__float_as_uint(hi)), 0x7632);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return (uint32_t)__bfloat16_as_ushort(h.x) | ((uint32_t)__bfloat16_as_ushort(h.y) << 16);
 }
 __device__ __forceinline__ float bf16_round_f32(float f) {
   return __uint_as_float(f32_to_bf16_bits(f) << 16);
@@ -411,6 +405,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// 8-byte global load cached in L2 only, issued where it stands (see below).
+__device__ __forceinline__ uint2 ldg_cg_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+// 16-byte global load cached in L2 only, issued where it stands: volatile,
+// so that the compiler neither sinks it towards its first use (a load meant
+// to be in flight during other work) nor merges it away.
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
 }
 
 // Ask for `bytes` (a multiple of 16, from a 16-byte aligned address) to be

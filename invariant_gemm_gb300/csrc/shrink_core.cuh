@@ -53,7 +53,7 @@ struct PartialArgs {
   uint32_t* status;
   const __nv_bfloat16* x;     // x [M][K]
   int64_t K;                  // row stride of x, in elements
-  int64_t Ks;                 // partition length
+  int Ks;                     // partition length (K < 2^31)
   int nrows;
   const CUtensorMap* tm_a;    // A as [rows][K], box 64 x BN, 128-byte swizzle
   const CUtensorMap* tm_a3;   // A as {64, rows, K/64}, box {64, BN, 4}, or null
@@ -90,7 +90,7 @@ struct PartialRing {
   using ARegs = uint4[NGW][kAF];   // A chunks (rows g, g + 8) of the same groups
 
   __device__ __forceinline__ int klen(const PartialArgs& a, int b) const {
-    return (int)min((int64_t)kShrinkKB, a.Ks - (int64_t)b * kShrinkKB);
+    return min(kShrinkKB, a.Ks - b * kShrinkKB);
   }
   __device__ __forceinline__ int nsub(const PartialArgs& a, int b) const {
     return (klen(a, b) + 63) / 64;
@@ -132,11 +132,9 @@ struct PartialRing {
     const int t = lane & 3;
 #pragma unroll
     for (int i = 0; i < NGW; ++i) {
-      const int64_t e = ((int64_t)kGroups * b + warp + W * i) * 64 + 16 * t;
-      xr[i][0] = e < a.Ks ? __ldcg(reinterpret_cast<const uint4*>(xrow + e))
-                          : make_uint4(0u, 0u, 0u, 0u);
-      xr[i][1] = e + 8 < a.Ks ? __ldcg(reinterpret_cast<const uint4*>(xrow + e + 8))
-                              : make_uint4(0u, 0u, 0u, 0u);
+      const int e = (kGroups * b + warp + W * i) * 64 + 16 * t;
+      xr[i][0] = e < a.Ks ? ldg_cg_v4(xrow + e) : make_uint4(0u, 0u, 0u, 0u);
+      xr[i][1] = e + 8 < a.Ks ? ldg_cg_v4(xrow + e + 8) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
   // This lane's A chunks of k-block b from stage st: chunks 2t, 2t+1 of rows
@@ -150,7 +148,7 @@ struct PartialRing {
 #pragma unroll
     for (int i = 0; i < NGW; ++i) {
       const int q = warp + W * i;                    // group within the k-block
-      const int64_t e = ((int64_t)kGroups * b + q) * 64 + 16 * t;
+      const int e = (kGroups * b + q) * 64 + 16 * t;
       const bool vlo = e < a.Ks, vhi = e + 8 < a.Ks;
       const uint32_t row = sa + q * BN * 128 + g * 128;
       const uint32_t clo = (uint32_t)(((2 * t) ^ g) << 4), chi = (uint32_t)(((2 * t + 1) ^ g) << 4);
@@ -169,7 +167,7 @@ struct PartialRing {
     const int warp = threadIdx.x >> 5;
 #pragma unroll
     for (int i = 0; i < NGW; ++i) {
-      if (((int64_t)kGroups * b + warp + W * i) * 64 >= a.Ks) continue;
+      if ((kGroups * b + warp + W * i) * 64 >= a.Ks) continue;
       const uint4& lo = ar[i][0];
       const uint4& hi = ar[i][1];
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   PartialArgs pa;
   pa.rows = rows_s;
   pa.status = p.status;
-  pa.Ks = p.Ks;
+  pa.Ks = (int)p.Ks;
   pa.nrows = nrows;
   pa.x = p.x;
   pa.K = p.K;

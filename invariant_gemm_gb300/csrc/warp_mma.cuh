@@ -6,7 +6,7 @@
 // Why warp-level MMA here and tcgen05 on the prefill path: a decode tile is
 // 8 tokens x 8 or 16 ranks. tcgen05.mma needs M >= 64 with both operands in
 // shared memory, so most of what it would read would be padding; m16n8k16 is
-// exactly 16 ranks x 8 tokens x 16 k (or 8 tokens x 8 columns x 16 ranks in
+// exactly 16 ranks x 8 tokens x 16 k (or 16 columns x 8 tokens x 16 ranks in
 // the expand), with its operands in registers.
 //
 // Fragment layouts (PTX ISA, mma.m16n8k16 / m16n8k8 with .bf16, .row.col),
@@ -71,106 +71,117 @@ __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t bf16_bits(float f) { return f32_to_bf16_bits(f); }
 
 // The expand on the tensor cores, one group of 32 output columns at a time:
-//   D[m][n] = sum over j of Zb[m][j] * B[n][j],  m < 8 (rows 8..15 zero)
-// j in increasing 16-element chunks (an 8-element chunk last when r % 16 ==
-// 8); with three Z parts (FP32 Z) the hi, mid and lo MMAs of a chunk follow
-// each other. A group is 4 MMAs of 8 columns (i = 0..3): column 2t' + e of
-// MMA i is the group's column 8t' + i + 4e, so that lane 4g + t ends with
-// the 8 consecutive columns 8t .. 8t+7 of row g (v[c] holds column 8t + c)
-// and updates them in y with one 16-byte load and one 16-byte store. Which
-// MMA computes a column does not change its value: every element is one
-// MMA's dot product over all of j, in the same order. Under the 128-byte
-// swizzle the 8 column addresses of one ldmatrix fall in 8 distinct bank
-// groups for r = 8 and r = 16.
+//   D[c][m] = sum over j of B[c][j] * Zb[m][j]   (c: 16 columns, m: 8 tokens)
+// one m16n8k16 per 16 columns and 16-element j chunk (m16n8k8 for a last 8),
+// the B rows as the A operand (ldmatrix from the swizzled B slice) and the
+// tile's Zb rows as the B operand (registers); j chunks in increasing order,
+// with three Z parts (FP32 Z) the hi, mid and lo MMAs of a chunk follow each
+// other. A group is 2 MMAs (h = 0, 1): MMA row g of MMA h is the group's
+// column 4g + 2h and row g + 8 its column 4g + 2h + 1, so that lane 4g + t
+// ends with columns 4g .. 4g+3 of tokens 2t (v[0..3]) and 2t + 1 (v[4..7]),
+// all four accumulator registers used, and updates them in y with one 8-byte
+// load and store per token. Which MMA computes a column does not change its
+// value: every element is one dot product over all of j, in the same order.
+// Under the 128-byte swizzle the 8 column addresses of one 8x8 matrix fall
+// in 8 distinct bank groups for r = 8 and r = 16.
 // zb: bf16 [parts][8][r] in shared memory; sB: the block's B columns,
 // column c at elements c * r .. c * r + r - 1 of a 128-byte-swizzled buffer
 // (see swz128); cb: the group's first column; columns past cmax are read as
 // column cmax (their results are not used).
-__device__ __forceinline__ int group_col(int cb, int i, int lane, int cmax) {
-  const int n = lane & 7;   // the MMA column whose B row address this lane gives
-  return min(cb + 8 * (n >> 1) + i + 4 * (n & 1), cmax);
-}
-
 __device__ __forceinline__ void expand_group_mma(float (&v)[8], uint32_t sB_addr, int cb,
                                                  int cmax, int r, const uint16_t* zb,
                                                  int parts, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const int jsel = ((lane >> 3) & 1) * 8;     // matrix 1: elements 8..15 of the chunk
+  const int mi = lane >> 3, rr = lane & 7;    // the 8x8 matrix and row this lane addresses
   const uint32_t* z32 = reinterpret_cast<const uint32_t*>(zb);
-  const int zrow = g * (r / 2);               // this lane's Z row, in bf16 pairs
+  const int zrow = g * (r / 2);               // token g's Z row, in bf16 pairs
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int h = 0; h < 2; ++h) {
     float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const int c = group_col(cb, i, lane, cmax);
+    const int c = min(cb + 4 * rr + (mi & 1) + 2 * h, cmax);
     int j = 0;
     for (; j + 16 <= r; j += 16) {
-      uint32_t b0, b1;
-      ldsm_x2(sB_addr + swz128((uint32_t)(c * r + j + jsel)), b0, b1);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(sB_addr + swz128((uint32_t)(c * r + j + (mi >> 1) * 8)), a0, a1, a2, a3);
 #pragma unroll 1
       for (int q = 0; q < parts; ++q) {
         const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
-        mma_16816(d, zp[0], 0u, zp[4], 0u, b0, b1);
+        mma_16816(d, a0, a1, a2, a3, zp[0], zp[4]);
       }
     }
     if (j < r) {   // last 8 elements
-      uint32_t b0;
-      ldsm_x1(sB_addr + swz128((uint32_t)(c * r + j)), b0);
+      uint32_t a0, a1;
+      ldsm_x2(sB_addr + swz128((uint32_t)(c * r + j)), a0, a1);
 #pragma unroll 1
       for (int q = 0; q < parts; ++q) {
         const uint32_t* zp = z32 + q * 4 * r + zrow + j / 2 + t;
-        mma_1688(d, zp[0], 0u, b0);
+        mma_1688(d, a0, a1, zp[0]);
       }
     }
-    v[i] = d[0];
-    v[4 + i] = d[1];
+    v[2 * h] = d[0];
+    v[2 * h + 1] = d[2];
+    v[4 + 2 * h] = d[1];
+    v[5 + 2 * h] = d[3];
   }
 }
 
 // The same MMAs as expand_group_mma for r = R (16 or 8) and one Z part,
-// split into operand loads and MMAs so that a warp can issue the loads of
-// several groups before their MMAs.
+// split into operand loads and MMAs, with the ldmatrix addresses computed
+// once per lane.
 template <int R>
 struct ExpandFrag {
-  uint32_t za0, za2;   // Zb fragment: row g, j 2t..2t+1 and j 2t+8..2t+9 (R = 16)
+  uint32_t zb0, zb1;   // Zb fragment: token g, j 2t..2t+1 and j 2t+8..2t+9 (R = 16)
   __device__ __forceinline__ void load_z(const uint16_t* zb, int lane) {
     const uint32_t* z32 = reinterpret_cast<const uint32_t*>(zb) + (lane >> 2) * (R / 2) +
                           (lane & 3);
-    za0 = z32[0];
-    za2 = R == 16 ? z32[4] : 0u;
+    zb0 = z32[0];
+    zb1 = R == 16 ? z32[4] : 0u;
   }
-  // B operands of the group's 4 MMAs
-  __device__ __forceinline__ static void load_b(uint32_t sB_addr, int cb, int cmax, int lane,
-                                                uint32_t (&b)[4][2]) {
+  // Byte offsets, from the start of a pair of groups in the B buffer, of the
+  // B rows this lane addresses in the 2 MMAs of a group of parity `par`:
+  // two groups span 64 columns x R elements = R 128-byte rows, a multiple of
+  // 8, so the swizzle pattern repeats from one pair to the next.
+  __device__ __forceinline__ static void lane_offsets(int lane, int par, uint32_t (&off)[2]) {
+    const int mi = lane >> 3, rr = lane & 7;
+    const int jsel = R == 16 ? (mi >> 1) * 8 : 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = group_col(cb, i, lane, cmax);
+    for (int h = 0; h < 2; ++h)
+      off[h] = swz128((uint32_t)((32 * par + 4 * rr + (mi & 1) + 2 * h) * R + jsel));
+  }
+  // A operands of the group whose pair starts at byte `base` of the B buffer
+  // (group g: base = sB + (g / 2) * 128 * R, offsets of parity g % 2); the
+  // buffer holds whole groups, so no column needs clamping.
+  __device__ __forceinline__ static void load_b_at(uint32_t base, const uint32_t (&off)[2],
+                                                   uint32_t (&a)[2][4]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
       if (R == 16) {
-        ldsm_x2(sB_addr + swz128((uint32_t)(c * R + ((lane >> 3) & 1) * 8)), b[i][0], b[i][1]);
+        ldsm_x4(base + off[h], a[h][0], a[h][1], a[h][2], a[h][3]);
       } else {
-        ldsm_x1(sB_addr + swz128((uint32_t)(c * R)), b[i][0]);
-        b[i][1] = 0u;
+        ldsm_x2(base + off[h], a[h][0], a[h][1]);
+        a[h][2] = a[h][3] = 0u;
       }
     }
   }
-  __device__ __forceinline__ void mma(float (&v)[8], const uint32_t (&b)[4][2]) const {
+  __device__ __forceinline__ void mma(float (&v)[8], const uint32_t (&a)[2][4]) const {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int h = 0; h < 2; ++h) {
       float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (R == 16) mma_16816(d, za0, 0u, za2, 0u, b[i][0], b[i][1]);
-      else mma_1688(d, za0, 0u, b[i][0]);
-      v[i] = d[0];
-      v[4 + i] = d[1];
+      if (R == 16) mma_16816(d, a[h][0], a[h][1], a[h][2], a[h][3], zb0, zb1);
+      else mma_1688(d, a[h][0], a[h][1], zb0);
+      v[2 * h] = d[0];
+      v[2 * h + 1] = d[2];
+      v[4 + 2 * h] = d[1];
+      v[5 + 2 * h] = d[3];
     }
   }
 };
 
-// y = bf16_rn(f32(y) + v) for 8 consecutive bf16 values (one rounding each).
-__device__ __forceinline__ uint4 y_add8(const uint4& y, const float (&v)[8]) {
-  uint4 o;
-  o.x = f32x2_to_bf16x2_bits(bf16lo(y.x) + v[0], bf16hi(y.x) + v[1]);
-  o.y = f32x2_to_bf16x2_bits(bf16lo(y.y) + v[2], bf16hi(y.y) + v[3]);
-  o.z = f32x2_to_bf16x2_bits(bf16lo(y.z) + v[4], bf16hi(y.z) + v[5]);
-  o.w = f32x2_to_bf16x2_bits(bf16lo(y.w) + v[6], bf16hi(y.w) + v[7]);
+// y = bf16_rn(f32(y) + v) for 4 consecutive bf16 values (one rounding each).
+__device__ __forceinline__ uint2 y_add4(const uint2& y, float v0, float v1, float v2, float v3) {
+  uint2 o;
+  o.x = f32x2_to_bf16x2_bits(bf16lo(y.x) + v0, bf16hi(y.x) + v1);
+  o.y = f32x2_to_bf16x2_bits(bf16lo(y.y) + v2, bf16hi(y.y) + v3);
   return o;
 }
 
