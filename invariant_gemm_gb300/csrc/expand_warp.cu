@@ -62,6 +62,9 @@ __host__ __device__ inline ExpandLayout expand_layout(int r, int64_t N) {
 
 __global__ void __launch_bounds__(kThreads, 2)
     expand_warp_kernel(const __grid_constant__ ExpandParams p) {
+  // the next kernel may be scheduled now: it reads nothing of ours before
+  // its own griddep_wait(), which waits for this grid to complete
+  griddep_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -107,7 +110,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (early_b) issue_b();
 
   griddep_wait();
-  griddep_launch();
   if (!early_b) issue_b();
 
   const int64_t M = p.M;

@@ -77,12 +77,15 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   return L;
 }
 
-// At most 128 registers a thread for BN = 16 (four blocks of 128 threads
-// per SM), so that the next layer's blocks fit beside this layer's and run
-// their prologue early.
+// At least four blocks per SM (at most 128 registers a thread for BN = 16),
+// so that the next layer's blocks fit beside this layer's and run their
+// prologue early.
 template <int BN>
-__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::THREADS)
+__global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 4)
     fused_warp_kernel(const __grid_constant__ FusedParams p) {
+  // the next kernel may be scheduled now: it reads nothing of ours before
+  // its own griddep_wait(), which waits for this grid to complete
+  griddep_launch();
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
   constexpr int W = ShrinkGeo<BN>::WARPS;
   constexpr int TB = FusedGeo<BN>::TB;
@@ -129,7 +132,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
   if (g == p.L) {
     // tokens without an adapter: zero Z rows, y untouched
     griddep_wait();
-    griddep_launch();
     if (s == 0)
       for (int i = tid; i < nrows * r; i += kThreads)
         p.z[((int64_t)sl * M + rows_s[i / r]) * r + i % r] = 0.0f;
@@ -225,7 +227,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
   const bool a_ok = fast ? ring.fast_prologue(pa, ar) : true;
 
   griddep_wait();
-  griddep_launch();
   if (warp == 0 && !early_w) {
     for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
     issue_b();
@@ -274,8 +275,14 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 512 / ShrinkGeo<BN>::T
     const int o = tid;
     uint16_t hi = 0, mid = 0, lo = 0;
     if (o < nrows * BN) {
+      // the S partials loaded together (S <= 16), then added in order
+      float pq[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) pq[q] = q < S ? part[q * TB + o] : 0.0f;
       float total = 0.0f;
-      for (int q = 0; q < S; ++q) total += part[q * TB + o];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q < S) total += pq[q];
       const float zv = total * p.scale;
       if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
       split_z(zv, zf32, hi, mid, lo);

@@ -32,6 +32,9 @@ __device__ __forceinline__ float tree_sum(float (&v)[kMaxS], int n) {
 }
 
 __global__ void __launch_bounds__(kThreads) reduce_tree_kernel(TreeParams p) {
+  // the next kernel may be scheduled now: it reads nothing of ours before
+  // its own griddep_wait(), which waits for this grid to complete
+  griddep_launch();
   int64_t bid = blockIdx.x;
   const int jb = (int)(bid % p.jblocks);
   bid /= p.jblocks;
@@ -42,7 +45,6 @@ __global__ void __launch_bounds__(kThreads) reduce_tree_kernel(TreeParams p) {
   const int g = ent[0];
   const int nrows = ent[1];
   griddep_wait();
-  griddep_launch();
   if (nrows <= 0 || g < 0 || g >= p.L) return;  // no-adapter rows were zeroed by the shrink
   const int64_t slot = (t * p.slices + sl) * p.jblocks + jb;
   const int64_t per = (int64_t)p.tile_rows * p.bn;     // partial values per split

@@ -54,6 +54,9 @@ struct ShrinkSmem {
 template <int BN, int MODE, bool CL>
 __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
     shrink_warp_kernel(const __grid_constant__ ShrinkParams p) {
+  // the next kernel may be scheduled now: it reads nothing of ours before
+  // its own griddep_wait(), which waits for this grid to complete
+  griddep_launch();
   using SM = ShrinkSmem<BN>;
   constexpr int kThreads = ShrinkGeo<BN>::THREADS;
   extern __shared__ uint8_t smem_raw[];
@@ -98,7 +101,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   if (g == p.L) {
     // tokens without an adapter: their Z rows are zero (ATOMIC zeroed Z already)
     griddep_wait();
-    griddep_launch();
     if (MODE != IG_MODE_ATOMIC && s == 0) {
       for (int i = tid; i < nrows * BN; i += kThreads) {
         const int row = i / BN, j = i % BN;
@@ -147,7 +149,6 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   typename PartialRing<BN>::ARegs ar[PartialRing<BN>::kFastKB];
   const bool a_ok = fast ? ring.fast_prologue(pa, ar) : true;
   griddep_wait();
-  griddep_launch();
   if (warp == 0 && !early_a)
     for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
   float v;
