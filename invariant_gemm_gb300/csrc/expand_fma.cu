@@ -38,9 +38,6 @@ static_assert(kExpandWarps * RW == kTileRows, "tile rows");
 // of 8. The chunking does not change the order of the j sum.
 template <int JC>
 __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p) {
-  // the next kernel may be scheduled now: it reads nothing of ours before
-  // its own griddep_wait(), which waits for this grid to complete
-  griddep_launch();
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   uint8_t* sB = smem + 128;
@@ -83,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
   if (early_b && warp == 0) issue_b();
 
   griddep_wait();
+  griddep_launch();
   if (!early_b && warp == 0) issue_b();
   const bool active = lane < groups && row0 < nrows;
   const int64_t n = n0 + lane * 8;

@@ -77,9 +77,6 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
 template <int BN>
 __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
     fused_fma_kernel(const __grid_constant__ FusedParams p) {
-  // the next kernel may be scheduled now: it reads nothing of ours before
-  // its own griddep_wait(), which waits for this grid to complete
-  griddep_launch();
   constexpr int kThreads = FmaGeo<BN>::THREADS;
   using F = FusedGeo<BN>;
   constexpr int CU = F::CU, CP = F::CP, TB = F::TB;
@@ -125,6 +122,7 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
   if (g == p.L) {
     // tokens without an adapter: zero Z rows, y untouched
     griddep_wait();
+    griddep_launch();
     if (s == 0)
       for (int i = tid; i < nrows * r; i += kThreads)
         p.z[((int64_t)sl * M + rows_s[i / r]) * r + i % r] = 0.0f;
@@ -180,6 +178,7 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
     if (early_w) issue_b();
   }
   griddep_wait();
+  griddep_launch();
   if (warp == 0) {
     for (int b = 0; b < first; ++b) {
       if (!early_w) ring.issue_a(pa, b);

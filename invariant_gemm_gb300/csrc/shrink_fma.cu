@@ -46,9 +46,6 @@ struct ShrinkSmem {
 template <int BN, int MODE>
 __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
     shrink_fma_kernel(const __grid_constant__ ShrinkParams p) {
-  // the next kernel may be scheduled now: it reads nothing of ours before
-  // its own griddep_wait(), which waits for this grid to complete
-  griddep_launch();
   using SM = ShrinkSmem<BN>;
   constexpr int kThreads = FmaGeo<BN>::THREADS;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -85,6 +82,7 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
   if (g == p.L) {
     // tokens without an adapter: their Z rows are zero (ATOMIC zeroed Z already)
     griddep_wait();
+    griddep_launch();
     if (MODE != IG_MODE_ATOMIC && s == 0) {
       for (int i = tid; i < nrows * BN; i += kThreads) {
         const int row = i / BN, j = i % BN;
@@ -123,6 +121,7 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
     }
   }
   griddep_wait();
+  griddep_launch();
   if (warp == 0) {
     for (int b = 0; b < first; ++b) {
       if (!early_a) ring.issue_a(pa, b);
