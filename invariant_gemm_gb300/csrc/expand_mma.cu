@@ -268,10 +268,9 @@ __global__ void __launch_bounds__(kThreads)
     const bool acc_ok = mbar_wait_bounded(&ctl->done[i & 1], (uint32_t)((i >> 1) & 1), p.status) &&
                         *reinterpret_cast<volatile int32_t*>(&ctl->fail) == 0;
     tc_fence_after();
-    if (__syncthreads_or(!(y_ok && acc_ok))) {
-      ok = false;
-      break;
-    }
+    // a thread whose own wait expired writes nothing; the block agrees on
+    // the failure at the barrier after the epilogue
+    const bool mine = y_ok && acc_ok;
     uint8_t* sy = stage(i) + ka * kBAtom;
 
     // epilogue 1: this thread's row: y = bf16_rn(f32(y) + acc), in shared memory
@@ -282,7 +281,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int c = 0; c < kBN; c += 32) {
         float v[32];
         tmem_ld32(trow + c, v);
-        if (m >= nrows) continue;
+        if (m >= nrows || !mine) continue;
         uint8_t* rowp = sy + (c / 64) * kYBox + m * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -301,11 +300,19 @@ __global__ void __launch_bounds__(kThreads)
     }
     tc_fence_before();
     fence_proxy_async_smem();
-    __syncthreads();
+    if (__syncthreads_or(!mine)) {
+      ok = false;
+      break;
+    }
 
-    // epilogue 2: back to global memory
+    // epilogue 2: back to global memory. A full tile of consecutive tokens
+    // goes by one TMA store that only thread 0 issues, so thread 0 alone
+    // frees the stage (after the store has read it) and refills it, with no
+    // block barrier; row stores read the stage from every thread, and a
+    // barrier follows them.
     const int ncols = (int)min((int64_t)kBN, N - n0 - (int64_t)i * kBN);
-    if (full_box && ncols == kBN) {
+    const bool tma_store = full_box && ncols == kBN;
+    if (tma_store) {
       if (tid == 0) {
         for (int yb = 0; yb < kYB; ++yb)
           tma_store_2d(&p.tm_yt, y_col + i * kBN + yb * 64, rows_s[0], sy + yb * kYBox);
@@ -323,8 +330,8 @@ __global__ void __launch_bounds__(kThreads)
           *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + yb * 64 +
                                     ch * 8) = u;
         }
+      __syncthreads();
     }
-    __syncthreads();
     // stage i % NS is free once the store has read it: copies of block i + NS
     if (i + NS < nb) {
       if (warp == 0) {
