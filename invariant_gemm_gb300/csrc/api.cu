@@ -198,9 +198,6 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
                          (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, kMmaExpandBN,
                          CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != IG_OK) return rc;
-  rc = encode_map_2d(&p.tm_y, y, (uint64_t)sh->M, (uint64_t)sh->slices * sh->N,
-                     (uint64_t)sh->slices * sh->N * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc != IG_OK) return rc;
   rc = encode_map_2d(&p.tm_yt, y, (uint64_t)sh->M, (uint64_t)sh->slices * sh->N,
                      (uint64_t)sh->slices * sh->N * 2, 64, kMmaTileRows,
                      CU_TENSOR_MAP_SWIZZLE_128B);

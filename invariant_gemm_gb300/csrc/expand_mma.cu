@@ -14,8 +14,9 @@
 // is built once per block (coalesced loads, written by the threads straight
 // into the 128-byte-swizzled K-major layout) and serves all its column
 // blocks. Per column block: the B operand (64 rows of B_i x r) and the y tile
-// (128 rows x 64 columns: one box when the tile's tokens are consecutive,
-// else row gathers) come by TMA into one of two stages, so the copies of
+// (128 rows x 64 columns: one TMA box when the tile's tokens are
+// consecutive, else 16-byte asynchronous copies by every thread) come into
+// one of two stages, so the copies of
 // block i+2 are in flight while block i is computed; tcgen05.mma, M = 128,
 // N = 64, K = 16 per instruction, r/16 of them, FP32 into one of two TMEM
 // accumulators. Each thread then reads its row of the accumulator, adds it to
@@ -65,6 +66,17 @@ __host__ __device__ inline size_t mma_expand_smem(int r, bool zf32) {
   return 1024 + off_stage(r, zf32, expand_stages(r));
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the arrival on
+// an mbarrier once every earlier such copy of this thread has landed.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1,
                                              const void* src) {
   asm volatile(
@@ -102,9 +114,13 @@ __global__ void __launch_bounds__(kThreads)
 
   for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
   if (tid == 0) {
+    // y of a tile of consecutive tokens comes by one TMA box (one arrival
+    // with its byte count); of scattered tokens, by 16-byte copies from
+    // every thread (one arrival each)
+    const bool contig = p.tiles[t * kMmaTileInts + 2] != 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&ctl->full_b[i], 1);
-      mbar_init(&ctl->full_y[i], 1);
+      mbar_init(&ctl->full_y[i], contig ? 1 : kThreads);
     }
     for (int i = 0; i < 2; ++i) mbar_init(&ctl->done[i], 1);
     ctl->fail = 0;
@@ -136,11 +152,10 @@ __global__ void __launch_bounds__(kThreads)
   const int nb = (int)min((int64_t)p.nb, (N - n0 + kBN - 1) / kBN);   // column blocks here
   const int b_row = (int)(((int64_t)g * p.slices + sl) * N + n0);
   const int y_col = (int)((int64_t)sl * N + n0);
-  const int groups4 = (nrows + 3) / 4;
   const bool contiguous = ent_s[2] != 0;   // rows are consecutive tokens: one box
   const bool full_box = contiguous && nrows == kMmaTileRows;
   const bool early_b = (p.flags & IG_FLAG_STATIC_WEIGHTS) != 0;
-  const uint32_t y_tx = kYB * (contiguous ? (uint32_t)kYBox : (uint32_t)groups4 * 4 * 128);
+  const uint32_t y_tx = kYB * (uint32_t)kYBox;
 
   // column block i: stage i % NS (phase (i / NS) & 1), accumulator i % 2
   // (phase (i / 2) & 1)
@@ -151,36 +166,42 @@ __global__ void __launch_bounds__(kThreads)
     for (int a = 0; a < ka; ++a)
       tma_load_2d(stage(i) + a * kBAtom, &p.tm_b, a * 64, b_row + i * kBN, &ctl->full_b[i % NS]);
   };
-  auto issue_y = [&](int i) {   // warp 0
+  // y tile of column block i into its stage, 128-byte swizzled (16-byte
+  // chunk c of row m at chunk c ^ (m % 8)). Consecutive tokens: one TMA box
+  // per 64 columns, thread 0. Scattered tokens: every thread copies 16-byte
+  // chunks (a warp instruction covers 4 rows x 128 bytes; columns past the
+  // block's ncols are not read) and arrives once its copies have landed; row
+  // gathers by TMA measured slower for scattered rows.
+  const int64_t ld = (int64_t)p.slices * N;
+  auto issue_y = [&](int i) {   // thread 0 (consecutive tokens) or every thread
     uint8_t* sy = stage(i) + ka * kBAtom;
-    if (lane == 0) mbar_arrive_expect_tx(&ctl->full_y[i % NS], y_tx);
-    __syncwarp();
     if (contiguous) {
-      if (lane == 0)
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&ctl->full_y[i % NS], y_tx);
         for (int yb = 0; yb < kYB; ++yb)
           tma_load_2d(sy + yb * kYBox, &p.tm_yt, y_col + i * kBN + yb * 64, rows_s[0],
                       &ctl->full_y[i % NS]);
+      }
       return;
     }
-    const int last = nrows - 1;
-    for (int q = lane; q < groups4 * kYB; q += 32) {
-      const int yb = q / groups4, g4 = q % groups4;
-      tma_gather4(sy + yb * kYBox + g4 * 512, &p.tm_y, y_col + i * kBN + yb * 64,
-                  rows_s[min(4 * g4, last)], rows_s[min(4 * g4 + 1, last)],
-                  rows_s[min(4 * g4 + 2, last)], rows_s[min(4 * g4 + 3, last)],
-                  &ctl->full_y[i % NS]);
+    const int nc = (int)min((int64_t)kBN, N - n0 - (int64_t)i * kBN);
+    const int ch = tid & 7;
+    for (int yb = 0; yb < kYB; ++yb) {
+      if (yb * 64 + ch * 8 >= nc) continue;
+      for (int m = tid >> 3; m < nrows; m += kThreads / 8)
+        cp_async16(sy + yb * kYBox + m * 128 + ((ch ^ (m & 7)) << 4),
+                   p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + yb * 64 + ch * 8);
     }
+    cp_async_mbar_arrive(&ctl->full_y[i % NS]);
   };
 
   if (tid == 0 && early_b)
     for (int i = 0; i < min(nb, NS); ++i) issue_b(i);
   griddep_wait();
   griddep_launch();
-  if (warp == 0) {
-    for (int i = 0; i < min(nb, NS); ++i) {
-      if (lane == 0 && !early_b) issue_b(i);
-      issue_y(i);
-    }
+  for (int i = 0; i < min(nb, NS); ++i) {
+    if (tid == 0 && !early_b) issue_b(i);
+    issue_y(i);
   }
 
   // A operand: the tile's Z rows rounded to bf16 into the swizzled K-major
@@ -252,7 +273,6 @@ __global__ void __launch_bounds__(kThreads)
   int next_mma = 0;   // thread 32: first block whose MMAs are not issued yet
   if (tid == 32) issue_mma(next_mma++, false);
 
-  const int64_t ld = (int64_t)p.slices * N;
   int issued = min(nb, NS);   // column blocks whose copies have been issued
   int i = 0;
   bool ok = true;
@@ -334,14 +354,11 @@ __global__ void __launch_bounds__(kThreads)
     }
     // stage i % NS is free once the store has read it: copies of block i + NS
     if (i + NS < nb) {
-      if (warp == 0) {
-        if (lane == 0) {
-          bulk_wait_read0();
-          issue_b(i + NS);
-        }
-        __syncwarp();
-        issue_y(i + NS);
+      if (tid == 0) {
+        bulk_wait_read0();
+        issue_b(i + NS);
       }
+      issue_y(i + NS);
       issued = i + NS + 1;
     }
     if (tid == 32 && next_mma == i + 1 && next_mma < nb) issue_mma(next_mma++, false);

@@ -155,7 +155,6 @@ struct MmaShrinkParams {
 
 struct MmaExpandParams {
   CUtensorMap tm_b;     // B_stack as [L*slices*N][r], box 64 x 64, 128-byte swizzle
-  CUtensorMap tm_y;     // y [M][slices*N], box 64 x 1, 128-byte swizzle (row gathers)
   CUtensorMap tm_yt;    // y [M][slices*N], box 64 x 128, 128-byte swizzle (contiguous tiles)
   const float* z;
   const int32_t* tiles; // 128-row tile table
