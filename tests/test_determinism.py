@@ -306,16 +306,20 @@ FUSED_CASES = [
 def test_fused_apply_bitwise_equals_two_kernels(case, path):
     """lora_apply's one-launch cluster kernel (DET) and the two-kernel path
     (Split-K shrink with the counter protocol, then expand) give the same bits
-    for z and y, on the warp-level tensor-core path and on the CUDA-core FMA
-    path; and both are within tolerance of the oracle."""
+    for z and y, with and without static weights, on the warp-level
+    tensor-core path and on the CUDA-core FMA path; and both are within
+    tolerance of the oracle."""
     M, K, N, r, slices, L, S, none_frac = case
     p = synth.make_problem(M, K, N, r, slices=slices, L=L, seed=M + K + S,
                            none_frac=none_frac, device="cuda")
     outs = []
-    for flags in (0, ig.FLAG_UNFUSED, ig.FLAG_STATIC_WEIGHTS):
+    # static weights: the A fragments of short partitions go into registers
+    # before the dependency wait (fused and two-kernel shrink alike)
+    for flags in (0, ig.FLAG_UNFUSED, ig.FLAG_STATIC_WEIGHTS,
+                  ig.FLAG_UNFUSED | ig.FLAG_STATIC_WEIGHTS):
         sh = ig.make_shape(M, K, N, r, slices=slices, num_adapters=L, split_k=S,
                            mode=ig.MODE_DET, path=path, flags=flags)
-        if flags != ig.FLAG_UNFUSED:
+        if not flags & ig.FLAG_UNFUSED:
             assert ig.plan_query(sh)["apply_kernels"] == 1
         z, y = run_apply(p, mode=ig.MODE_DET, split_k=S, ws=ig.workspace(sh),
                          shape=sh)
