@@ -416,13 +416,24 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank-line runs (string literals
+    in these files hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_hash(name):
-    """Hash of the sources a kernel is compiled from (its .cu and headers)."""
+    """Hash of the code a kernel is compiled from (its .cu and headers,
+    comments left out, so that a recorded ncu capture stays tied to the
+    kernel's code and not to the wording around it)."""
     h = hashlib.sha256()
     try:
         for f in KERNEL_SOURCES.get(name, [name]):
-            with open(os.path.join(ROOT, "invariant_gemm_gb300", "csrc", f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(ROOT, "invariant_gemm_gb300", "csrc", f)) as fh:
+                h.update(_code_only(fh.read()).encode())
     except OSError:
         return None
     return h.hexdigest()[:16]

@@ -28,11 +28,13 @@
 // (r = 8 or 16). Copies: the A rows of the partition by TMA (128-byte
 // swizzled, one 3-D copy per 256 elements), and the block's B column slice
 // by tiled TMA copies of 128-byte rows (64/r columns x r ranks each), both
-// issued before griddep_wait when the weights are static; x and y go
-// straight from global memory into registers in 16-byte loads right after
-// the wait (L2 was asked for the block's x and y rows before it), so that y
-// arrives while the shrink computes. Both the shrink partial and the expand
-// run on the warp-level tensor cores.
+// issued before griddep_wait when the weights are static (and then, for a
+// partition of at most two k-blocks, this lane's A chunks are read into
+// registers before the wait too); x and y go straight from global memory
+// into registers right after the wait, x in 16-byte and y in 8-byte loads
+// (L2 was asked for the block's x and y rows before it), so that y arrives
+// while the shrink computes. Both the shrink partial and the expand run on
+// the warp-level tensor cores.
 #include "shrink_core.cuh"
 
 namespace ig {
