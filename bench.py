@@ -800,7 +800,9 @@ def main():
            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": det["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic", "config": workload_config(), "clocks": clk,
-           "gpu_launches": launches * args.steps,
+           # this library's kernels in the headline's timed region: the
+           # deterministic step (token map + one fused launch per layer)
+           "gpu_launches": graphs["det_sk8"][1] * args.steps,
            "roofline": roofline, "variants": results, "sweep_M": sweep, "split_sweep": split_sweep,
            "atomic_replay": replay, "single_call": single, "prefill": prefill,
            "e2e": e2e,
