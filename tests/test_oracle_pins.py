@@ -422,11 +422,17 @@ def _mut_expand(kind):
                 continue
             rows = np.nonzero(idx == a)[0]
             for sl in range(slices):
-                Bas = B[a, sl]
+                Bas = B[(a + 1) % L if kind == "wrong_adapter" else a, sl]
                 cols = slice(sl * N, (sl + 1) * N)
                 if kind == "slice_swapped":
                     Bas = B[a, (sl + 1) % slices]
+                if kind == "b_strided":     # B read as [r][N] instead of [N][r]
+                    Bas = Bas.reshape(r, N).T
                 add = zb[sl, rows] @ Bas.T
+                if kind == "scaled_twice":
+                    add = 2.0 * add
+                if kind == "n_reversed":
+                    add = add[:, ::-1]
                 if kind == "y_dropped":
                     y_exact[rows, cols] = add
                 else:
@@ -435,6 +441,9 @@ def _mut_expand(kind):
         out = np.asarray(y_bits).astype(np.uint16).copy()
         if kind == "none_touched":
             out = oracle.bf16_round(y_exact)
+        elif kind == "y_truncated":   # final conversion drops the low bits
+            act = idx >= 0
+            out[act] = (y_exact[act].astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
         else:
             act = idx >= 0
             out[act] = oracle.bf16_round(y_exact[act])
@@ -456,7 +465,8 @@ def test_planted_shrink_mistakes_are_caught(kind):
 
 
 @pytest.mark.parametrize("kind", ["no_z_rounding", "z_truncated", "none_touched",
-                                  "slice_swapped", "y_dropped"])
+                                  "slice_swapped", "y_dropped", "wrong_adapter",
+                                  "b_strided", "scaled_twice", "n_reversed", "y_truncated"])
 def test_planted_expand_mistakes_are_caught(kind):
     mut = _mut_expand(kind)
     caught = []
