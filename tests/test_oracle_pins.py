@@ -388,7 +388,10 @@ def _mut_shrink(kind):
                 s = 1.0 if kind == "no_scale" else scale
                 if kind == "sign":
                     s = -s
-                zz = s * (x[rows] @ Aas.T)
+                if kind == "scale_squared":
+                    s = scale * scale
+                xr = x[np.roll(rows, 1)] if kind == "rows_rolled" else x[rows]
+                zz = s * (xr @ Aas.T)
                 if kind == "j_reversed":
                     zz = zz[:, ::-1]
                 z[sl, rows] = zz
@@ -452,7 +455,8 @@ def _mut_expand(kind):
 
 
 @pytest.mark.parametrize("kind", ["wrong_adapter", "dropped_term", "transposed",
-                                  "no_scale", "sign", "j_reversed"])
+                                  "no_scale", "sign", "j_reversed", "scale_squared",
+                                  "rows_rolled"])
 def test_planted_shrink_mistakes_are_caught(kind):
     mut = _mut_shrink(kind)
     caught = []
