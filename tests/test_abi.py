@@ -111,6 +111,7 @@ def test_workspace_bytes():
     (dict(num_adapters=5000), -9), (dict(r=512), -9),
     (dict(mode=3, split_k=128), -9),
     (dict(r=256, path=2, flags=4), -9),        # three bf16 Z parts do not fit at r = 256
+    (dict(K=2**31), -9), (dict(N=2**31), -9),  # 32-bit tensor-map coordinates
 ])
 def test_plan_rejects(kw, code):
     with pytest.raises(ig.IGError) as e:
