@@ -295,81 +295,210 @@ def kernel_durations(ig, st, ws, steps):
     return out
 
 
-PREFILL = [
-    # name, M, K, N, r, slices, L, adapter ids, S, instances
-    # Split-K per shape, the fastest measured of 1 / 2 / 4 / 8 (QKV, slices
-    # stacked in one MMA: apply 114 / 94 / 81 / 74 us; down: 104 / 68 / 56 /
-    # 54 us)
-    ("qkv_M4096_K4096_r64_3x4096", 4096, 4096, 4096, 64, 3, 16, "segments", 8, 2),
-    ("down_M4096_K11008_r64_N4096", 4096, 11008, 4096, 64, 1, 16, "segments", 8, 2),
-    # Split-K 4 for the large-model shapes: of the allowed 1, 4, 8, 16 the
-    # fastest measured (cluster combine, M = 8192: 98 / 110 / 164 us at
-    # S = 4 / 8 / 16 for K = 8192)
-    ("large_M8192_K8192_r128_N8192", 8192, 8192, 8192, 128, 1, 64, "zipf", 4, 2),
-    ("large_M8192_K28672_r128_N8192", 8192, 28672, 8192, 128, 1, 64, "zipf", 4, 1),
-]
+def decode_independent(ig, st, device, steps, nstreams=8):
+    """The decode layer stack with the layers as independent work: the 64
+    distinct-buffer lora_apply calls run as `nstreams` independent branches
+    of one CUDA graph (layer l on branch l % nstreams, each branch with its
+    own workspace, token map and z), so that one layer's dependency latency
+    overlaps other layers' memory traffic. Same workload, same kernels, same
+    results as the dependent chain; it shows what the fused kernel sustains
+    when its latency can be hidden. Returns step time, tokens/s and the
+    algorithmic bandwidth of the 64 layers."""
+    sh = make_shape(ig, st, ig.MODE_DET)
+    wss = [ig.workspace(sh, device=device) for _ in range(nstreams)]
+    zs = [torch.empty_like(st.z) for _ in range(nstreams)]
+    streams = [torch.cuda.Stream() for _ in range(nstreams)]
 
+    def body():
+        cur = torch.cuda.current_stream()
+        for b in range(nstreams):
+            streams[b].wait_stream(cur)
+            with torch.cuda.stream(streams[b]):
+                ig.map_tokens(sh, st.idx, wss[b], streams[b])
+                for l in range(b, st.layers, nstreams):
+                    ig.lora_apply(sh, st.x[l], st.y[l], None, st.A[l], st.B[l], st.scale,
+                                  zs[b], wss[b], streams[b])
+        for b in range(nstreams):
+            cur.wait_stream(streams[b])
 
-def prefill_bench(ig, device, steps):
-    """Prefill shapes on the tensor-core path: per lora_apply time, algorithmic
-    HBM GB/s and TFLOP/s, and the shrink / expand split (each kernel alone in
-    its own graph). Distinct instances per shape keep the inputs out of L2."""
-    import synth
-    out = {}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    ms = time_graph(g, steps, 3, 1, device)
+    for w in wss:
+        assert ig.check_status(w) == 0
+    b = alg_bytes(st.M, st.K, st.N, st.r, st.slices, st.u)
+    gbs = b["total"] * st.layers / (ms * 1e-3) / 1e9
     peak, kind = measured_peaks()
-    for name, M, K, N, r, sl, L, ids, S, inst in PREFILL:
-        probs = [synth.make_problem(M, K, N, r, slices=sl, L=L, ids=ids, segment=256,
-                                    seed=4000 + i, device=device) for i in range(inst)]
-        sh = ig.make_shape(M, K, N, r, slices=sl, num_adapters=L, split_k=S, mode=ig.MODE_DET,
-                           flags=ig.FLAG_STATIC_WEIGHTS)
-        info = ig.plan_query(sh)
-        ws = ig.workspace(sh, device=device)
-        z = torch.empty((sl, M, r), dtype=torch.float32, device=device)
-        ig.map_tokens(sh, probs[0].idx, ws)
-        u = int(torch.unique(probs[0].idx).numel())
-        b = alg_bytes(M, K, N, r, sl, u)
-        flops = 2 * M * K * r * sl + 2 * M * r * N * sl
-        res = {"path": "tcgen05" if info["path"] == ig.PATH_MMA else "warp", "split_k": S}
-        for part in ("apply", "shrink", "expand"):
-            def body(stream, part=part):
-                for p in probs:
-                    if part == "apply":
-                        ig.lora_apply(sh, p.x, p.y, None, p.A, p.B, p.scale, z, ws, stream)
-                    elif part == "shrink":
-                        ig.lora_shrink(sh, p.x, p.A, None, p.scale, z, ws, stream)
-                    else:
-                        ig.lora_expand(sh, z, p.B, None, p.y, ws, stream)
-            st = torch.cuda.Stream()
-            st.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(st):
-                body(st)
-            torch.cuda.current_stream().wait_stream(st)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                body(torch.cuda.current_stream())
-            for _ in range(3):
-                g.replay()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
+    del g
+    return {"branches": nstreams, "layers_per_branch": st.layers // nstreams,
+            "ms_per_step": ms, "us_per_layer": ms * 1e3 / st.layers,
+            "tokens_per_s": st.M * st.layers / (ms * 1e-3), "hbm_gbs": gbs,
+            "hbm_frac_of_" + kind: gbs / peak,
+            "launches_per_step": nstreams + st.layers * ig.plan_query(sh)["apply_kernels"],
+            "how": "64 distinct-buffer lora_apply calls (DET, Split-K 8) as independent "
+                   "branches of one CUDA graph, one workspace, token map and z per branch; "
+                   "algorithmic bytes of the 64 layers over the step time"}
+
+
+# Prefill workloads on the tcgen05 path.
+# Stacked QKV and MLP down-projection at M = 4096 (16 adapters in contiguous
+# 256-token segments; Split-K 8 as the workload states, plus the Split-K
+# sweep of sec. 4), and the large-model skinny GEMMs (K = 8192 hidden and
+# K = 28672 down-projection, r = 128, N = 8192, 64 adapters with Zipf(1.1)
+# token frequencies) over M in {1, 16, 256, 2048, 8192} and Split-K in
+# {1, 4, 8, 16}.
+PREFILL_STACKED = [
+    # name, M, K, N, r, slices, L, adapter ids
+    ("qkv_M4096_K4096_r64_3x4096", 4096, 4096, 4096, 64, 3, 16, "segments"),
+    ("down_M4096_K11008_r64_N4096", 4096, 11008, 4096, 64, 1, 16, "segments"),
+]
+LARGE_K = [8192, 28672]
+LARGE_M = [1, 16, 256, 2048, 8192]
+LARGE_S = [1, 4, 8, 16]
+L2_FLUSH_BYTES = 320 << 20        # larger than the 129 MB L2
+
+
+class CallTimer:
+    """Device time of one call captured in a CUDA graph, L2 flushed before
+    every timed replay (the flush is outside the events): median over reps."""
+
+    def __init__(self, device):
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def time(self, body, reps, warm=3):
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            body(st)
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body(torch.cuda.current_stream())
+        for _ in range(warm):
+            self.flush.fill_(0)
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for e0, e1 in ev:
+            self.flush.fill_(0)
             e0.record()
-            for _ in range(steps):
-                g.replay()
+            g.replay()
             e1.record()
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (steps * inst)
-            nbytes = b["total"] if part == "apply" else b[part]
-            nfl = flops if part == "apply" else (2 * M * K * r * sl if part == "shrink"
-                                                 else 2 * M * r * N * sl)
-            res[part] = {"us": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
-                         "hbm_frac_of_" + kind: nbytes / (us * 1e-6) / 1e9 / peak,
-                         "tflops": nfl / (us * 1e-6) / 1e12,
-                         "tokens_per_s": M / (us * 1e-6)}
-            del g
+        torch.cuda.synchronize()
+        del g
+        return statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)   # us
+
+
+def _point(us, M, nbytes, flops, peak, kind):
+    return {"us": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
+            "hbm_frac_of_" + kind: nbytes / (us * 1e-6) / 1e9 / peak,
+            "tflops": flops / (us * 1e-6) / 1e12, "tokens_per_s": M / (us * 1e-6)}
+
+
+# (name, mode, extra flags): on the tcgen05 path the deterministic shrink
+# combines its partials inside a thread-block cluster by default, and with
+# IG_FLAG_UNFUSED through the workspace with the completion counter
+# (Algorithm 1); both are one shrink launch and one expand launch.
+PREFILL_VARIANTS = (("det_cluster", 0, 0), ("det_counter", 0, 2), ("atomic", 1, 0))
+
+
+def prefill_bench(ig, device, reps):
+    """Prefill workloads on the tensor-core path: per lora_apply device time,
+    algorithmic HBM GB/s and its fraction of the measured peak, TFLOP/s and
+    tokens/s for deterministic Split-K (cluster combine and counter
+    protocol), atomic Split-K and unsplit; for the stacked workloads also the
+    shrink / expand split and a Split-K sweep of the deterministic path."""
+    import synth
+    peak, kind = measured_peaks()
+    timer = CallTimer(device)
+    out = {"timing": "one lora_apply per CUDA-graph replay, L2 flushed (320 MB write) "
+                     "before each replay outside the events; median of the replays",
+           "stacked": {}, "large": {}}
+
+    def run_points(p, M, specs, ws, z):
+        """specs: list of (key, mode, flags, S, part)."""
+        u = int(torch.unique(p.idx[:M][p.idx[:M] >= 0]).numel())
+        b = alg_bytes(M, p.K, p.N, p.r, p.slices, u)
+        fl = {"shrink": 2 * M * p.K * p.r * p.slices, "expand": 2 * M * p.r * p.N * p.slices}
+        fl["apply"] = fl["shrink"] + fl["expand"]
+        b["apply"] = b["total"]
+        res = {}
+        for key, mode, flags, S, part in specs:
+            sh = ig.make_shape(M, p.K, p.N, p.r, slices=p.slices, num_adapters=p.L, split_k=S,
+                               mode=mode, flags=ig.FLAG_STATIC_WEIGHTS | flags)
+            ig.map_tokens(sh, p.idx[:M], ws)
+            x, y, zz = p.x[:M], p.y[:M], z[:, :M]
+
+            def body(stream, part=part):
+                if part == "apply":
+                    ig.lora_apply(sh, x, y, None, p.A, p.B, p.scale, zz, ws, stream)
+                elif part == "shrink":
+                    ig.lora_shrink(sh, x, p.A, None, p.scale, zz, ws, stream)
+                else:
+                    ig.lora_expand(sh, zz, p.B, None, y, ws, stream)
+            us = timer.time(body, reps)
+            res[key] = _point(us, M, b[part], fl[part], peak, kind)
+            res[key]["split_k"] = 1 if mode == ig.MODE_UNSPLIT else S
         assert ig.check_status(ws) == 0
-        out[name] = res
-        del probs, ws, z
+        return res
+
+    def overheads(res, tag):
+        o = {}
+        if "atomic" + tag in res:
+            a = res["atomic" + tag]["us"]
+            for k in ("det_cluster", "det_counter"):
+                if k + tag in res:
+                    o[k + "_vs_atomic_pct"] = 100 * (res[k + tag]["us"] / a - 1)
+        if "unsplit" in res and "det_cluster" + tag in res:
+            o["det_cluster_speedup_vs_unsplit_pct"] = 100 * (
+                res["unsplit"]["us"] / res["det_cluster" + tag]["us"] - 1)
+        return o
+
+    for name, M, K, N, r, sl, L, ids in PREFILL_STACKED:
+        p = synth.make_problem(M, K, N, r, slices=sl, L=L, ids=ids, segment=256, seed=4000,
+                               device=device)
+        ws = ig.workspace(ig.make_shape(M, K, N, r, slices=sl, num_adapters=L, split_k=16),
+                          device=device)
+        z = torch.empty((sl, M, r), dtype=torch.float32, device=device)
+        specs = [(f"{v}_sk8", m, f, 8, "apply") for v, m, f in PREFILL_VARIANTS]
+        specs.append(("unsplit", ig.MODE_UNSPLIT, 0, 1, "apply"))
+        specs += [(f"det_cluster_sk{S}", 0, 0, S, "apply") for S in (2, 4, 16)]
+        specs += [("det_cluster_sk8_shrink", 0, 0, 8, "shrink"),
+                  ("det_cluster_sk8_expand", 0, 0, 8, "expand")]
+        res = run_points(p, M, specs, ws, z)
+        res["overhead"] = overheads(res, "_sk8")
+        res["path"] = "tcgen05" if ig.plan_query(
+            ig.make_shape(M, K, N, r, slices=sl, num_adapters=L))["path"] == ig.PATH_MMA \
+            else "warp"
+        out["stacked"][name] = res
+        del p, ws, z
+        torch.cuda.empty_cache()
+
+    for K in LARGE_K:
+        Mx, N, r, L = max(LARGE_M), 8192, 128, 64
+        p = synth.make_problem(Mx, K, N, r, L=L, ids="zipf", seed=4100 + K, device=device)
+        ws = ig.workspace(ig.make_shape(Mx, K, N, r, num_adapters=L, split_k=16),
+                          device=device)
+        z = torch.empty((1, Mx, r), dtype=torch.float32, device=device)
+        for M in LARGE_M:
+            specs = [("unsplit", ig.MODE_UNSPLIT, 0, 1, "apply")]
+            for S in LARGE_S:
+                specs += [(f"{v}_sk{S}", m, f, S, "apply") for v, m, f in PREFILL_VARIANTS]
+            res = run_points(p, M, specs, ws, z)
+            res["overhead"] = {f"sk{S}": overheads(res, f"_sk{S}") for S in LARGE_S}
+            best = min((k for k in res if k.startswith("det_cluster_sk")),
+                       key=lambda k: res[k]["us"])
+            res["fastest_det"] = best
+            out["large"][f"K{K}_M{M}"] = res
+        del p, ws, z
         torch.cuda.empty_cache()
     return out
 
@@ -508,7 +637,111 @@ def oracle_all_cores(seconds):
     return sum(t for t, _ in res), n
 
 
-def cpu_baseline_obj(seconds):
+# The workloads' configurations for the per-configuration oracle timing:
+# (name, M, K, N, r, slices, L, adapter ids, rows timed per call). Large
+# configurations are timed on a sample of their rows (the oracle's cost is
+# per row), with only the sample's adapters handed to it.
+CPU_CONFIGS = [
+    ("single_adapter_M4_K512_r8_N512", 4, 512, 512, 8, 1, 1, "uniform", 4),
+    ("decode_M256_K4096_r16_N4096", 256, 4096, 4096, 16, 1, 8, "uniform", 256),
+    ("prefill_qkv_M4096_K4096_r64_3x4096", 4096, 4096, 4096, 64, 3, 16, "segments", 64),
+    ("prefill_down_M4096_K11008_r64_N4096", 4096, 11008, 4096, 64, 1, 16, "segments", 64),
+    ("batch_invariance_M1024_K4096_r32_N4096", 1024, 4096, 4096, 32, 1, 32, "uniform", 128),
+    ("large_M8192_K8192_r128_N8192", 8192, 8192, 8192, 128, 1, 64, "zipf", 32),
+    ("large_M8192_K28672_r128_N8192", 8192, 28672, 8192, 128, 1, 64, "zipf", 16),
+]
+
+
+def _cfg_sample(cfg, seed):
+    """Host inputs of `rows` tokens drawn from the configuration (adapter ids
+    from its distribution over the full batch, the first `rows` kept), with
+    A and B holding only the adapters those rows use."""
+    import synth
+    name, M, K, N, r, sl, L, ids, rows = cfg
+    g = torch.Generator().manual_seed(seed)
+    idx_full = synth.adapter_ids(M, L, ids, g, "cpu")
+    idx = idx_full[:rows]
+    used = torch.unique(idx[idx >= 0])
+    remap = torch.full((L,), -1, dtype=torch.int32)
+    remap[used.long()] = torch.arange(used.numel(), dtype=torch.int32)
+    p = synth.make_problem(rows, K, N, r, slices=sl, L=max(1, used.numel()), seed=seed,
+                           device="cpu")
+
+    def b(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    return (b(p.x), b(p.y), remap[idx.long()].numpy(), b(p.A), b(p.B))
+
+
+def _oracle_cfg_time(cfg, seconds, seed=11):
+    import oracle
+    x, y, idx, A, B = _cfg_sample(cfg, seed)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.apply(x, y, idx, A, B, 2.0)
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return cfg[8] * done / dt, done
+
+
+def _oracle_cfg_worker(seconds, seed, barrier, q):
+    # one process per core: every configuration in turn, all processes
+    # starting each configuration together
+    res = []
+    for cfg in CPU_CONFIGS:
+        barrier.wait(timeout=600)
+        res.append(_oracle_cfg_time(cfg, seconds, seed))
+    q.put(res)
+
+
+def host_info():
+    info = {"nproc": os.cpu_count()}
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() in ("Model name", "Architecture", "CPU(s)", "Vendor ID"):
+                info[k.strip()] = v.strip()
+    except Exception as e:
+        info["lscpu"] = f"unavailable: {e}"[:120]
+    return info
+
+
+def cpu_per_config(seconds):
+    """The FP64 oracle (as it stands) timed on every configuration, one core
+    and all cores (one spawned process per core, each on its own sample,
+    every configuration started by all of them together). tokens/s = rows of
+    the sample x calls / time."""
+    import multiprocessing as mp
+    out = {}
+    for cfg in CPU_CONFIGS:
+        one, done = _oracle_cfg_time(cfg, seconds)
+        out[cfg[0]] = {"one_core_tokens_per_s": one, "sample_rows": cfg[8], "calls": done}
+    n = os.cpu_count() or 1
+    try:
+        ctx = mp.get_context("spawn")
+        q = ctx.Queue()
+        bar = ctx.Barrier(n)
+        procs = [ctx.Process(target=_oracle_cfg_worker, args=(seconds, 11 + i, bar, q))
+                 for i in range(n)]
+        for pr in procs:
+            pr.start()
+        res = [q.get(timeout=len(CPU_CONFIGS) * (seconds * 6 + 60) + 120) for _ in procs]
+        for pr in procs:
+            pr.join(timeout=60)
+        for c, cfg in enumerate(CPU_CONFIGS):
+            out[cfg[0]]["all_cores_tokens_per_s"] = sum(r[c][0] for r in res)
+            out[cfg[0]]["all_cores"] = n
+    except Exception as e:
+        for cfg in CPU_CONFIGS:
+            out[cfg[0]]["all_cores_unavailable"] = str(e)[:200]
+    return out
+
+
+def cpu_baseline_obj(seconds, per_config=0.0):
     v, done, threads = oracle_sample(seconds)
     out = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
            "sample": f"{done} layers of the workload (M={WORKLOAD['M']}, K={WORKLOAD['K']}, "
@@ -520,6 +753,14 @@ def cpu_baseline_obj(seconds):
                             "how": "one process per host core, same sample each"}
     except Exception as e:   # the one-core number stands on its own
         out["all_cores"] = {"unavailable": str(e)[:200]}
+    out["host"] = host_info()
+    if per_config:
+        out["per_config"] = cpu_per_config(per_config)
+        out["per_config_how"] = (
+            f"FP64 numpy oracle, shrink+expand, ~{per_config:.1f} s per configuration on one "
+            "core and the same on every core at once (one spawned process per core, one "
+            "BLAS thread each); large configurations on a sample of their rows with only "
+            "those rows' adapters; tokens/s = sample rows x calls / time")
     return out
 
 
@@ -572,7 +813,9 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-config-seconds", type=float, default=2.0,
+                    help="oracle time per configuration (0: skip the per-configuration table)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--replays", type=int, default=200,
@@ -794,7 +1037,9 @@ def main():
             single[name][f"M{Mx}_us"] = ms * 1e3
             del g1
 
-    prefill = {} if args.no_prefill else prefill_bench(ig, device, max(5, args.steps // 40))
+    independent = {str(n): decode_independent(ig, st, device, max(20, args.steps // 4), n)
+                   for n in (4, 8)}
+    prefill = {} if args.no_prefill else prefill_bench(ig, device, 7)
 
     out = {"metric": METRIC, "value": det["tokens_per_s"], "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": det["ms_per_step"],
@@ -805,10 +1050,11 @@ def main():
            "gpu_launches": graphs["det_sk8"][1] * args.steps,
            "roofline": roofline, "variants": results, "sweep_M": sweep, "split_sweep": split_sweep,
            "atomic_replay": replay, "single_call": single, "prefill": prefill,
+           "decode_independent_layers": independent,
            "e2e": e2e,
            "hbm_gbs": det["hbm_gbs"]}
     if rank == 0:
-        out["cpu_baseline"] = cpu_baseline_obj(args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline_obj(args.cpu_seconds, args.cpu_config_seconds)
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist

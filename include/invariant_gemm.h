@@ -155,6 +155,19 @@ typedef struct ig_shape {
                                     per step of the rank sum; FMA path: Z
                                     used as stored. */
 
+#define IG_FLAG_TEST_COPY_TIMEOUT 8 /* For testing the timeout path only; never
+                                    set it in production. Warp-path shrink
+                                    kernels (lora_shrink, and lora_apply's
+                                    fused kernel) give their first A-copy wait
+                                    no time at all: each block checks that
+                                    copy once, right after issuing it, finds it
+                                    still in flight, records IG_ERR_TIMEOUT,
+                                    waits (bounded) for its own copies to land
+                                    and leaves. The call's z and y are then
+                                    unspecified, and ig_check_status reports
+                                    IG_ERR_TIMEOUT and re-zeroes the counters.
+                                    Not part of the determinism key. */
+
 /* The resolved plan. Everything that fixes the arithmetic is in
  * determinism_key, which never depends on M. */
 typedef struct ig_plan_info {
@@ -222,9 +235,13 @@ int lora_shrink(const ig_shape* shape, const void* x, const void* A_stack,
  *                             + sum_{j<r} bf16_rn(z[sl][m][j]) * B_stack[a_m][sl][n][j] )
  * (with IG_FLAG_Z_FP32: z[sl][m][j] itself instead of bf16_rn(z); the
  * tensor-core paths feed it as three bf16 parts that sum to it exactly)
- * The sum over j is a sequential FP32 chain in increasing j; y is rounded
- * once. Rows with adapter -1 are not written. adapter_idx may be NULL to
- * reuse the token map in ws. */
+ * The sum over j is an FP32 sum whose order is fixed by r and the path, not
+ * by M: on the tensor-core paths (IG_PATH_WARP, IG_PATH_MMA) the rank axis
+ * is taken in chunks of 16 in increasing order, one MMA per chunk, each
+ * adding its 16 products into the FP32 accumulator inside the tensor core;
+ * on IG_PATH_FMA a sequential FMA chain in increasing j. y is rounded once.
+ * Rows with adapter -1 are not written. adapter_idx may be NULL to reuse the
+ * token map in ws. */
 int lora_expand(const ig_shape* shape, const float* z, const void* B_stack,
                 const int32_t* adapter_idx, void* y,
                 void* ws, size_t ws_bytes, void* stream);
@@ -272,7 +289,10 @@ int lora_shrink_noalloc(const ig_shape* shape, const void* x, const void* A_stac
  * the most severe device-side error recorded since the last check
  * (IG_ERR_TIMEOUT, IG_ERR_WS_CORRUPT, IG_ERR_ADAPTER_RANGE) or IG_OK. After
  * IG_ERR_WS_CORRUPT or IG_ERR_TIMEOUT the completion counters are zeroed
- * again, so the workspace is usable for the next call. */
+ * again, so the workspace is usable for the next call. After IG_ERR_TIMEOUT
+ * the z and y written by the calls since the last check are unspecified
+ * (a block whose wait expired contributed nothing, or zeros); every block
+ * still waited, bounded, for its own copies before it left. */
 int ig_check_status(void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus

@@ -116,8 +116,11 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
   };
   load_z(0);
   // every thread waits for the B slice, so the block never exits with copies
-  // in flight
-  if (!mbar_wait_bounded(bar, 0, p.status)) return;
+  // in flight; after an expired wait, once more (bounded) before it leaves
+  if (!mbar_wait_bounded(bar, 0, p.status)) {
+    mbar_wait_bounded(bar, 0, p.status);
+    return;
+  }
   if (!active) return;
 
   float acc[RW][8];

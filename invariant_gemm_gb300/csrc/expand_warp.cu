@@ -145,8 +145,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   // every thread waits for the B slice, so the block never exits with copies
-  // in flight
-  if (!mbar_wait_bounded(bar, 0, p.status)) return;
+  // in flight; after an expired wait, once more (bounded) before it leaves
+  if (!mbar_wait_bounded(bar, 0, p.status)) {
+    mbar_wait_bounded(bar, 0, p.status);
+    return;
+  }
 
   const uint32_t sB_addr = smem_u32(sB);
   const int parts = zf32 ? 3 : 1;

@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 4)
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)((int64_t)s * p.Ks);
   pa.a_row = (int)(((int64_t)g * p.slices + sl) * r);
+  pa.first_budget = first_copy_budget(p.flags);
   PartialRing<BN> ring;
   ring.stages = smem + lay.ring_off;
   ring.bars = bars;

@@ -291,11 +291,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking check of an mbarrier phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase. Gives up after ~2^31 SM clocks (about a
-// second), records kStatusTimeout and returns false.
+// second), records kStatusTimeout and returns false. A budget of 0 or less
+// checks the phase once without waiting (IG_FLAG_TEST_COPY_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint32_t* status,
                                                   long long budget = 1ll << 31) {
+  if (budget <= 0) {
+    if (mbar_test_wait(bar, parity)) return true;
+    atomicOr(status, kStatusTimeout);
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {

@@ -58,6 +58,12 @@ extern "C" int lora_shrink_noalloc(const ig_shape* shape, const void* x, const v
   if (rc != IG_OK) return rc;
   if (shape->M == 0) return IG_OK;
   if (!adapter_idx) return IG_ERR_ARG;  // no map survives between calls by contract
+  // The argument checks lora_shrink makes, made here before the clear below
+  // is enqueued: a rejected call enqueues nothing.
+  if (!x || !A_stack || !z) return IG_ERR_ARG;
+  auto aligned16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
+  if (!aligned16(x) || !aligned16(A_stack) || !aligned16(z) || !aligned16(adapter_idx))
+    return IG_ERR_ALIGN;
   if ((size_t)info.workspace_bytes > kNoAllocScratchBytes) return IG_ERR_WS_SMALL;
   void* ws = nullptr;
   rc = scratch_for_current_device(&ws);

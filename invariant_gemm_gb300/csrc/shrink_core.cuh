@@ -59,7 +59,14 @@ struct PartialArgs {
   const CUtensorMap* tm_a3;   // A as {64, rows, K/64}, box {64, BN, 4}, or null
   int k0;                     // partition start (column coordinate)
   int a_row;                  // row coordinate of the tile's first A row
+  long long first_budget;     // budget of the first A-copy wait (clocks; <= 0:
+                              // one check, IG_FLAG_TEST_COPY_TIMEOUT)
 };
+
+// Budget of a block's first A-copy wait for the given ig_shape flags.
+__host__ __device__ inline long long first_copy_budget(int flags) {
+  return (flags & IG_FLAG_TEST_COPY_TIMEOUT) ? 0ll : (1ll << 31);
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -221,7 +228,8 @@ struct PartialRing {
     bool ok = true;
 #pragma unroll
     for (int b = 0; b < kFastKB; ++b) {
-      if (b < nkb && ok) ok = mbar_wait_bounded(&bars[b], 0u, a.status);
+      if (b < nkb && ok)
+        ok = mbar_wait_bounded(&bars[b], 0u, a.status, b == 0 ? a.first_budget : 1ll << 31);
       if (b < nkb && ok) load_a(a, b, b, ar[b]);
     }
     return ok;
@@ -266,7 +274,9 @@ struct PartialRing {
       if (b + 1 < nkb) load_x(xrow, a, b + 1, xn);
       if (b == 0) after_first_x();
       const int st = b % nst;
-      if (ok) ok = mbar_wait_bounded(&bars[st], (uint32_t)((b / nst) & 1), a.status);
+      if (ok)
+        ok = mbar_wait_bounded(&bars[st], (uint32_t)((b / nst) & 1), a.status,
+                               b == 0 ? a.first_budget : 1ll << 31);
       if (ok) {
         ARegs ar;
         load_a(a, st, b, ar);

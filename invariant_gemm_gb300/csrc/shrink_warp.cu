@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS)
   pa.tm_a3 = p.has_a3 ? &p.tm_a3 : nullptr;
   pa.k0 = (int)k0;
   pa.a_row = (int)(((int64_t)g * p.slices + sl) * r + (int64_t)jb * BN);
+  pa.first_budget = first_copy_budget(p.flags);
   PartialRing<BN> ring;
   ring.stages = stages;
   ring.bars = bars;

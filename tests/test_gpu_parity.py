@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import invariant_gemm_gb300 as ig
+import oracle
 import synth
 from helpers import (bits, check_expand, check_shrink, need_gpu, run_apply, shape_of)
 
@@ -108,8 +109,28 @@ def test_prefill_sampled_rows(which, mode):
     check_expand(cpu(p), z, y, rows=rows)
 
 
-LARGE = [(8192, 1, 8), (8192, 256, 8), (8192, 2048, 4), (28672, 16, 16), (28672, 8192, 16),
-         (28672, 256, 1)]
+# (K, M, S) of the large-model workload (K = 8192 hidden, K = 28672 down-
+# projection; M in {1, 16, 256, 2048, 8192}; Split-K in {1, 4, 8, 16}): every
+# M at K = 8192 and at K = 28672, every Split-K at each K.
+LARGE = [(8192, 1, 8), (8192, 1, 16), (8192, 16, 4), (8192, 16, 16), (8192, 256, 8),
+         (8192, 2048, 4), (8192, 8192, 8), (8192, 8192, 16), (8192, 8192, 1),
+         (28672, 1, 4), (28672, 16, 16), (28672, 256, 1), (28672, 2048, 8),
+         (28672, 8192, 16), (28672, 8192, 8)]
+
+
+def _sub_problem(p, rows):
+    """The sampled rows of a device problem on the host, with only the
+    adapters those rows use (renumbered), so that the oracle stays small."""
+    rt = torch.as_tensor(rows, device="cuda")
+    idx = p.idx[rt].cpu()
+    used = torch.unique(idx[idx >= 0]).long()
+    remap = torch.full((p.L,), -1, dtype=torch.int32)
+    remap[used] = torch.arange(used.numel(), dtype=torch.int32)
+    ud = used.to("cuda")
+    return synth.Problem(M=len(rows), K=p.K, N=p.N, r=p.r, slices=p.slices,
+                         L=max(1, used.numel()), scale=p.scale, x=p.x[rt].cpu(),
+                         A=p.A[ud].cpu(), B=p.B[ud].cpu(), y=p.y[rt].cpu(),
+                         idx=torch.where(idx >= 0, remap[idx.clamp(min=0).long()], idx)), rt
 
 
 @pytest.mark.parametrize("K,M,S", LARGE)
@@ -119,15 +140,32 @@ def test_large_model_sampled_rows(K, M, S, mode):
         pytest.skip("Split-K = 1 has nothing to add atomically")
     p = synth.make_problem(M, K, 8192, 128, L=64, ids="zipf", seed=1004, device="cuda")
     z, y = run_apply(p, mode=mode, split_k=S)
-    rows = _sample_rows(M, 24, K + M)
-    # the oracle only needs the sampled rows; keep the host copies small
-    sub = synth.Problem(M=len(rows), K=K, N=p.N, r=p.r, slices=1, L=p.L, scale=p.scale,
-                        x=p.x[torch.as_tensor(rows, device="cuda")].cpu(), A=p.A.cpu(),
-                        B=p.B.cpu(), y=p.y[torch.as_tensor(rows, device="cuda")].cpu(),
-                        idx=p.idx[torch.as_tensor(rows, device="cuda")].cpu())
-    rt = torch.as_tensor(rows, device="cuda")
+    sub, rt = _sub_problem(p, _sample_rows(M, 24, K + M))
     check_shrink(sub, z[:, rt])
     check_expand(sub, z[:, rt], y[rt])
+
+
+@pytest.mark.parametrize("variant", ["det_cluster", "det_counter", "atomic", "unsplit"])
+def test_large_model_integers_bit_exact(variant):
+    """K = 28672, r = 128 on tcgen05 with small-integer x, A, B, y: every
+    partial sum of the shrink is an integer below 28672 * 16 < 2^24, so every
+    order gives the exact value and z must equal the oracle's bit for bit;
+    the expand's sums are integers too (bf16(z) has at most 8 significant
+    bits), and where the oracle's sum of magnitudes stays below 2^24 y must
+    equal bf16(y_exact) bit for bit."""
+    mode, flags = {"det_cluster": (ig.MODE_DET, 0), "det_counter": (ig.MODE_DET, ig.FLAG_UNFUSED),
+                   "atomic": (ig.MODE_ATOMIC, 0), "unsplit": (ig.MODE_UNSPLIT, 0)}[variant]
+    p = synth.make_problem(512, 28672, 8192, 128, L=64, ids="zipf", dist="int", seed=1014,
+                           device="cuda")
+    sh = ig.make_shape(p.M, p.K, p.N, p.r, num_adapters=p.L, split_k=8, mode=mode, flags=flags)
+    assert ig.plan_query(sh)["path"] == ig.PATH_MMA
+    z, y = run_apply(p, shape=sh)
+    sub, rt = _sub_problem(p, _sample_rows(p.M, 40, 28672))
+    check_shrink(sub, z[:, rt], exact=True)
+    _, bound, _ = oracle.expand(z[:, rt].cpu().numpy(), bits(sub.B), sub.idx.numpy(),
+                                bits(sub.y))
+    assert float(bound.max()) < 2.0 ** 24
+    check_expand(sub, z[:, rt], y[rt], exact=True)
 
 
 def test_zero_tokens():
