@@ -367,10 +367,18 @@ L2_FLUSH_BYTES = 320 << 20        # larger than the 129 MB L2
 
 class CallTimer:
     """Device time of one call captured in a CUDA graph, L2 flushed before
-    every timed replay (the flush is outside the events): median over reps."""
+    every timed replay (outside the events): median over reps. The flush
+    writes a buffer larger than L2 and then reads it back, so that the timed
+    call starts with L2 holding only clean, unrelated lines (it neither hits
+    in L2 nor pays for writing back the flush's dirty lines)."""
 
     def __init__(self, device):
-        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+        torch.sum(self.flush_buf, dim=0, out=self.sink)
 
     def time(self, body, reps, warm=3):
         st = torch.cuda.Stream()
@@ -383,12 +391,12 @@ class CallTimer:
         with torch.cuda.graph(g):
             body(torch.cuda.current_stream())
         for _ in range(warm):
-            self.flush.fill_(0)
+            self.flush()
             g.replay()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)]
         for e0, e1 in ev:
-            self.flush.fill_(0)
+            self.flush()
             e0.record()
             g.replay()
             e1.record()
@@ -419,8 +427,9 @@ def prefill_bench(ig, device, reps):
     import synth
     peak, kind = measured_peaks()
     timer = CallTimer(device)
-    out = {"timing": "one lora_apply per CUDA-graph replay, L2 flushed (320 MB write) "
-                     "before each replay outside the events; median of the replays",
+    out = {"timing": "one lora_apply per CUDA-graph replay; before each replay, outside "
+                     "the events, a 320 MB buffer is written and read back (L2 flushed, "
+                     "left clean); median of the replays",
            "stacked": {}, "large": {}}
 
     def run_points(p, M, specs, ws, z):
