@@ -207,31 +207,47 @@ __global__ void __launch_bounds__(kThreads)
   // A operand: the tile's Z rows rounded to bf16 into the swizzled K-major
   // layout (16-byte chunk c of a 128-byte row m sits at chunk c ^ (m % 8)),
   // rows past nrows zero. Warp w loads rows 32w .. 32w+31, r/4 lanes per row
-  // (4 values each, coalesced). With FP32 Z also mid = bf16_rn(z - hi) and
-  // lo = bf16_rn(z - hi - mid) (hi + mid + lo == z exactly), in atoms after
-  // the hi ones.
+  // (4 values each, coalesced), 16 loads in flight per lane before any is
+  // used (one at a time, each load's latency under the copies in flight
+  // added up to most of the block's life). With FP32 Z also
+  // mid = bf16_rn(z - hi) and lo = bf16_rn(z - hi - mid) (hi + mid + lo == z
+  // exactly), in atoms after the hi ones.
   {
     const int per_row = r / 4;
-    for (int idx = lane; idx < 32 * per_row; idx += 32) {
-      const int m = warp * 32 + idx / per_row;
-      const int j = 4 * (idx % per_row);
-      float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (m < nrows) f = __ldcg(reinterpret_cast<const float4*>(p.z + ((int64_t)sl * M + rows_s[m]) * r + j));
-      const float fv[4] = {f.x, f.y, f.z, f.w};
-      uint32_t pt[3][4];   // bf16 parts hi, mid, lo
+    const int total = 32 * per_row;           // float4 of the warp's 32 rows
+    for (int b0 = 0; b0 < total; b0 += 16 * 32) {
+      float4 f4[16];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint16_t h, md, l;
-        split_z(fv[e], zf32, h, md, l);
-        pt[0][e] = h;
-        pt[1][e] = md;
-        pt[2][e] = l;
+      for (int k = 0; k < 16; ++k) {
+        const int idx = b0 + lane + 32 * k;
+        const int m = warp * 32 + idx / per_row;
+        f4[k] = idx < total && m < nrows
+                    ? __ldcg(reinterpret_cast<const float4*>(
+                          p.z + ((int64_t)sl * M + rows_s[m]) * r + 4 * (idx % per_row)))
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
-      const int a = j / 64, c = (j % 64) / 8;
-      const size_t off = (size_t)a * 16384 + m * 128 + ((c ^ (m & 7)) << 4) + (j % 8) * 2;
-      for (int q = 0; q < (zf32 ? 3 : 1); ++q)
-        *reinterpret_cast<uint2*>(s_zb + (size_t)q * ka * 16384 + off) =
-            make_uint2(pt[q][0] | (pt[q][1] << 16), pt[q][2] | (pt[q][3] << 16));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int idx = b0 + lane + 32 * k;
+        if (idx >= total) continue;
+        const int m = warp * 32 + idx / per_row;
+        const int j = 4 * (idx % per_row);
+        const float fv[4] = {f4[k].x, f4[k].y, f4[k].z, f4[k].w};
+        uint32_t pt[3][4];   // bf16 parts hi, mid, lo
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint16_t h, md, l;
+          split_z(fv[e], zf32, h, md, l);
+          pt[0][e] = h;
+          pt[1][e] = md;
+          pt[2][e] = l;
+        }
+        const int a = j / 64, c = (j % 64) / 8;
+        const size_t off = (size_t)a * 16384 + m * 128 + ((c ^ (m & 7)) << 4) + (j % 8) * 2;
+        for (int q = 0; q < (zf32 ? 3 : 1); ++q)
+          *reinterpret_cast<uint2*>(s_zb + (size_t)q * ka * 16384 + off) =
+              make_uint2(pt[q][0] | (pt[q][1] << 16), pt[q][2] | (pt[q][3] << 16));
+      }
     }
     // rank columns past r inside the last atom are zero
     if (r % 64) {
