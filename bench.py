@@ -256,9 +256,16 @@ def kernel_durations(ig, st, ws, steps):
     ig.map_tokens(fused, st.idx, ws)
     torch.cuda.synchronize()
 
+    ready = make_shape(ig, st, ig.MODE_DET, extra_flags=ig.FLAG_INPUT_READY)
+
     def fused_only(stream):
         for l in range(st.layers):
             ig.lora_apply(fused, st.x[l], st.y[l], None, st.A[l], st.B[l], st.scale, st.z,
+                          ws, stream)
+
+    def fused_ready(stream):
+        for l in range(st.layers):
+            ig.lora_apply(ready, st.x[l], st.y[l], None, st.A[l], st.B[l], st.scale, st.z,
                           ws, stream)
 
     def shrink_only(stream):
@@ -270,7 +277,8 @@ def kernel_durations(ig, st, ws, steps):
             ig.lora_expand(two, st.z, st.B[l], None, st.y[l], ws, stream)
 
     out = {}
-    for name, fn in (("fused", fused_only), ("shrink", shrink_only), ("expand", expand_only)):
+    for name, fn in (("fused", fused_only), ("fused_input_ready", fused_ready),
+                     ("shrink", shrink_only), ("expand", expand_only)):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -484,6 +492,9 @@ def prefill_bench(ig, device, reps):
                   ("det_cluster_sk8_expand", 0, 0, 8, "expand")]
         res = run_points(p, M, specs, ws, z)
         res["overhead"] = overheads(res, "_sk8")
+        wk = f"{name},S=8"
+        res["det_cluster_sk8_shrink"]["traffic"] = ncu_traffic("shrink_mma.cu", wk)
+        res["det_cluster_sk8_expand"]["traffic"] = ncu_traffic("expand_mma.cu", wk)
         res["path"] = "tcgen05" if ig.plan_query(
             ig.make_shape(M, K, N, r, slices=sl, num_adapters=L))["path"] == ig.PATH_MMA \
             else "warp"
@@ -506,6 +517,9 @@ def prefill_bench(ig, device, reps):
             best = min((k for k in res if k.startswith("det_cluster_sk")),
                        key=lambda k: res[k]["us"])
             res["fastest_det"] = best
+            if K == 8192 and M == 8192:
+                res["expand_kernel_traffic"] = ncu_traffic(
+                    "expand_mma.cu", "large_M8192_K8192_r128_N8192,S=4")
             out["large"][f"K{K}_M{M}"] = res
         del p, ws, z
         torch.cuda.empty_cache()
@@ -551,6 +565,8 @@ KERNEL_SOURCES = {
     "fused_warp.cu": ["fused_warp.cu", "shrink_core.cuh", "warp_mma.cuh", "ig_common.cuh"],
     "shrink_warp.cu": ["shrink_warp.cu", "shrink_core.cuh", "warp_mma.cuh", "ig_common.cuh"],
     "expand_warp.cu": ["expand_warp.cu", "warp_mma.cuh", "ig_common.cuh"],
+    "shrink_mma.cu": ["shrink_mma.cu", "umma.cuh", "ig_common.cuh"],
+    "expand_mma.cu": ["expand_mma.cu", "umma.cuh", "ig_common.cuh"],
 }
 
 
@@ -579,12 +595,14 @@ def source_hash(name):
 
 def ncu_traffic(kernel_file, workload_key):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of that kernel and on this workload; else None."""
+    the current source of that kernel and on this workload; else None.
+    Entries are keyed by kernel file, or by "file|workload" where one kernel
+    has captures on several workloads."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d[kernel_file]
+        e = d.get(kernel_file + "|" + workload_key) or d[kernel_file]
         if e.get("source_sha256_16") != source_hash(kernel_file):
             return None
         if e.get("workload") != workload_key:
@@ -784,6 +802,53 @@ def workload_config():
             "l2": "inputs larger than L2 (distinct tensors per layer, 384 MB per step)"}
 
 
+PROFILE_CASES = {
+    # name: (M, K, N, r, slices, L, adapter ids, Split-K, entry point)
+    "qkv-shrink": (4096, 4096, 4096, 64, 3, 16, "segments", 8, "shrink"),
+    "qkv-expand": (4096, 4096, 4096, 64, 3, 16, "segments", 8, "expand"),
+    "scattered-expand": (8192, 8192, 8192, 128, 1, 64, "zipf", 4, "expand"),
+}
+
+
+def profile_case(name):
+    """A few calls of one kernel on a fixed workload, for ncu captures (no
+    timing): the decode layer stack (32 layers of the bench workload, two
+    passes of lora_apply), or a prefill shape's shrink or expand (three
+    calls after one warm-up shrink)."""
+    import synth
+    import invariant_gemm_gb300 as ig
+    device = torch.device("cuda", 0)
+    if name == "decode":
+        W = WORKLOAD
+        st = Stack(W["M"], W["K"], W["N"], W["r"], W["slices"], W["L"], 32, W["scale"],
+                   seed=1001, device=device)
+        sh = make_shape(ig, st, ig.MODE_DET)
+        ws = ig.workspace(sh, device=device)
+        ig.map_tokens(sh, st.idx, ws)
+        for _ in range(2):
+            for l in range(st.layers):
+                ig.lora_apply(sh, st.x[l], st.y[l], None, st.A[l], st.B[l], st.scale, st.z, ws)
+    else:
+        M, K, N, r, sl, L, ids, S, part = PROFILE_CASES[name]
+        p = synth.make_problem(M, K, N, r, slices=sl, L=L, ids=ids, segment=256, seed=4000,
+                               device=device)
+        sh = ig.make_shape(M, K, N, r, slices=sl, num_adapters=L, split_k=S,
+                           flags=ig.FLAG_STATIC_WEIGHTS)
+        ws = ig.workspace(sh, device=device)
+        z = torch.empty((sl, M, r), dtype=torch.float32, device=device)
+        ig.map_tokens(sh, p.idx, ws)
+        ig.lora_shrink(sh, p.x, p.A, None, p.scale, z, ws)
+        for _ in range(3):
+            if part == "shrink":
+                ig.lora_shrink(sh, p.x, p.A, None, p.scale, z, ws)
+            else:
+                ig.lora_expand(sh, z, p.B, None, p.y, ws)
+    torch.cuda.synchronize()
+    assert ig.check_status(ws) == 0
+    print(f"profile case {name}: ok")
+    return 0
+
+
 def reference_main(args, rank, world):
     if rank != 0:
         return 0
@@ -829,8 +894,12 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--replays", type=int, default=200,
                     help="identical-input replays per variant for the mismatch statistics")
+    ap.add_argument("--profile-case", choices=["decode"] + sorted(PROFILE_CASES),
+                    help="run a few calls of one kernel on a fixed workload (for ncu) and exit")
     args = ap.parse_args()
     rank, world, local = dist_env()
+    if args.profile_case:
+        return profile_case(args.profile_case)
 
     if args.impl == "reference":
         return reference_main(args, rank, world)
@@ -856,6 +925,7 @@ def main():
     # (name, mode, flags, path): the default (warp-level tensor-core) path in
     # every mode, and the CUDA-core FMA path as its baseline
     variants = (("det_sk8", ig.MODE_DET, 0, ig.PATH_AUTO),
+                ("det_sk8_input_ready", ig.MODE_DET, ig.FLAG_INPUT_READY, ig.PATH_AUTO),
                 ("det_sk8_two_kernel", ig.MODE_DET, ig.FLAG_UNFUSED, ig.PATH_AUTO),
                 ("det_tree_sk8_two_launch", ig.MODE_DET_TREE, 0, ig.PATH_AUTO),
                 ("atomic_sk8", ig.MODE_ATOMIC, 0, ig.PATH_AUTO),
@@ -898,6 +968,8 @@ def main():
                                                    det["ms_per_step"] - 1)
     results["det_tree_overhead_vs_det_pct"] = 100 * (
         results["det_tree_sk8_two_launch"]["ms_per_step"] / det["ms_per_step"] - 1)
+    results["input_ready_speedup_pct"] = 100 * (
+        det["ms_per_step"] / results["det_sk8_input_ready"]["ms_per_step"] - 1)
 
     # sweep over the decode batch sizes
     sweep = {}
@@ -935,6 +1007,8 @@ def main():
     kd = kernel_durations(ig, st, ws[ig.MODE_DET], max(20, args.steps // 4))
     b = alg_bytes(W["M"], W["K"], W["N"], W["r"], W["slices"], st.u)
     kern = {"fused_warp (lora_apply, det)": (kd["fused"], b["total"], "fused_warp.cu"),
+            "fused_warp (lora_apply, det, input ready)": (kd["fused_input_ready"], b["total"],
+                                                          "fused_warp.cu"),
             "shrink_warp (lora_shrink alone, det, cluster combine)": (kd["shrink"],
                                                                       b["shrink"],
                                                                       "shrink_warp.cu"),
@@ -1033,7 +1107,9 @@ def main():
     single = {}
     st1 = Stack(1, W["K"], W["N"], W["r"], W["slices"], W["L"], 1, W["scale"], seed=5,
                 device=device)
-    for name, mode, fl, path in variants[:5]:
+    for name, mode, fl, path in [v for v in variants if v[0] in (
+            "det_sk8", "det_sk8_two_kernel", "det_tree_sk8_two_launch", "atomic_sk8",
+            "unsplit_sk1")]:
         single[name] = {}
         for Mx, stx in ((1, st1), (W["M"], st)):
             sh = make_shape(ig, stx, mode, extra_flags=fl, path=path)
@@ -1048,6 +1124,12 @@ def main():
 
     independent = {str(n): decode_independent(ig, st, device, max(20, args.steps // 4), n)
                    for n in (4, 8)}
+    best = max(independent.values(), key=lambda v: v["hbm_gbs"])
+    roofline["independent_layers"] = {
+        "achieved": best["hbm_gbs"], "peak": peak, "unit": "GB/s",
+        "frac": best["hbm_gbs"] / peak, "branches": best["branches"],
+        "how": "the same 64 layers as independent graph branches (fused kernel, DET); "
+               "algorithmic bytes of 64 layers over the step time"}
     prefill = {} if args.no_prefill else prefill_bench(ig, device, 7)
 
     out = {"metric": METRIC, "value": det["tokens_per_s"], "unit": UNIT, "n_gpus": world,

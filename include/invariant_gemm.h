@@ -155,6 +155,18 @@ typedef struct ig_shape {
                                     per step of the rank sum; FMA path: Z
                                     used as stored. */
 
+#define IG_FLAG_INPUT_READY 16   /* With IG_FLAG_STATIC_WEIGHTS: x is not written
+                                    by any work still running on `stream`
+                                    when the call is enqueued (true when x is
+                                    the input of a base GEMM that runs just
+                                    before the LoRA call, or comes from an
+                                    earlier layer). The fused decode kernel
+                                    then runs its shrink, partial exchange
+                                    and combine while the previous kernel on
+                                    the stream is still finishing; z and y
+                                    are still read and written only after it
+                                    has completed. Same results; not part of
+                                    the determinism key. */
 #define IG_FLAG_TEST_COPY_TIMEOUT 8 /* For testing the timeout path only; never
                                     set it in production. Warp-path shrink
                                     kernels (lora_shrink, and lora_apply's

@@ -21,6 +21,7 @@ import os
 __all__ = [
     "MODE_DET", "MODE_ATOMIC", "MODE_UNSPLIT", "MODE_DET_TREE", "PATH_AUTO", "PATH_WARP", "PATH_MMA", "PATH_FMA",
     "FLAG_STATIC_WEIGHTS", "FLAG_UNFUSED", "FLAG_Z_FP32", "FLAG_TEST_COPY_TIMEOUT",
+    "FLAG_INPUT_READY",
     "IGError", "Shape", "PlanInfo", "lib", "lib_path", "make_shape", "workspace_bytes",
     "plan_query", "workspace", "workspace_init", "map_tokens", "lora_shrink",
     "lora_expand", "lora_apply", "lora_shrink_noalloc", "check_status", "status_string",
@@ -32,6 +33,7 @@ FLAG_STATIC_WEIGHTS = 1
 FLAG_UNFUSED = 2
 FLAG_Z_FP32 = 4
 FLAG_TEST_COPY_TIMEOUT = 8   # testing only: the first A-copy wait of each block expires
+FLAG_INPUT_READY = 16        # x not written by work still running on the stream
 PATH_AUTO, PATH_WARP, PATH_MMA, PATH_FMA = 0, 1, 2, 3
 
 STATUS = {

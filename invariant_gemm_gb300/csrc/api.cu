@@ -40,7 +40,7 @@ uint64_t fnv1a(uint64_t h, int64_t v) {
 int make_plan(const ig_shape* sh, Plan* pl) {
   if (!sh || !pl) return IG_ERR_ARG;
   if ((sh->flags & ~(IG_FLAG_STATIC_WEIGHTS | IG_FLAG_UNFUSED | IG_FLAG_Z_FP32 |
-                     IG_FLAG_TEST_COPY_TIMEOUT)) != 0)
+                     IG_FLAG_TEST_COPY_TIMEOUT | IG_FLAG_INPUT_READY)) != 0)
     return IG_ERR_ARG;
   if (sh->mode < IG_MODE_DET || sh->mode > IG_MODE_DET_TREE) return IG_ERR_ARG;
   if (sh->path < IG_PATH_AUTO || sh->path > IG_PATH_FMA) return IG_ERR_ARG;

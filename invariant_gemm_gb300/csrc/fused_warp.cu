@@ -229,15 +229,21 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 4)
   typename PartialRing<BN>::ARegs ar[PartialRing<BN>::kFastKB];
   const bool a_ok = fast ? ring.fast_prologue(pa, ar) : true;
 
-  griddep_wait();
+  // With IG_FLAG_INPUT_READY (and static weights) x is not written by the
+  // kernel before this one on the stream: the shrink, the partial exchange
+  // and the combine run before the dependency wait, and only the z store and
+  // the y update (reads included) follow it.
+  const bool pre = early_w && (p.flags & IG_FLAG_INPUT_READY) != 0;
+  if (!pre) griddep_wait();
   if (warp == 0 && !early_w) {
     for (int b = 0; b < first; ++b) ring.issue_a(pa, b);
     issue_b();
   }
   uint2 ypre[kGB][2];
   float v;
-  const bool ok = fast ? ring.fast_run(pa, xrow, ar, a_ok, red, v, [&]() { load_y(0, ypre); })
-                       : ring.run(pa, xrow, red, v, [&]() { load_y(0, ypre); });
+  const bool ok = fast ? ring.fast_run(pa, xrow, ar, a_ok, red, v,
+                                       [&]() { if (!pre) load_y(0, ypre); })
+                       : ring.run(pa, xrow, red, v, [&]() { if (!pre) load_y(0, ypre); });
 
   // Send this block's partial P_s to slot s of every block of the cluster
   // (its own included). Every block sends on every path (zeros after a
@@ -274,6 +280,7 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 4)
 
   // Combine (Algorithm 1 order): total = 0; total += P_q for q = 0..S-1.
   // Thread o owns output o (token row o / r, rank o % r).
+  float zv = 0.0f;
   {
     const int o = tid;
     uint16_t hi = 0, mid = 0, lo = 0;
@@ -286,14 +293,18 @@ __global__ void __launch_bounds__(ShrinkGeo<BN>::THREADS, 4)
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         if (q < S) total += pq[q];
-      const float zv = total * p.scale;
-      if (s == 0) p.z[((int64_t)sl * M + rows_s[o / BN]) * r + o % BN] = zv;
+      zv = total * p.scale;
       split_z(zv, zf32, hi, mid, lo);
     }
     zb[o] = hi;
     zb[TB + o] = mid;
     zb[2 * TB + o] = lo;
   }
+  if (pre) {
+    griddep_wait();
+    load_y(0, ypre);
+  }
+  if (s == 0 && tid < nrows * BN) p.z[((int64_t)sl * M + rows_s[tid / BN]) * r + tid % BN] = zv;
   __syncthreads();   // zb complete
 
   // Expand this block's columns: y = bf16_rn(f32(y) + D), D the tensor-core
