@@ -161,12 +161,16 @@ typedef struct ig_shape {
                                     the input of a base GEMM that runs just
                                     before the LoRA call, or comes from an
                                     earlier layer). The fused decode kernel
-                                    then runs its shrink, partial exchange
-                                    and combine while the previous kernel on
-                                    the stream is still finishing; z and y
-                                    are still read and written only after it
-                                    has completed. Same results; not part of
-                                    the determinism key. */
+                                    of the warp path (lora_apply with
+                                    ig_plan_info.apply_kernels == 1, not
+                                    IG_PATH_FMA) then runs its shrink,
+                                    partial exchange and combine while the
+                                    previous kernel on the stream is still
+                                    finishing; z and y are still read and
+                                    written only after it has completed.
+                                    Other kernels ignore the flag. Same
+                                    results; not part of the determinism
+                                    key. */
 #define IG_FLAG_TEST_COPY_TIMEOUT 8 /* For testing the timeout path only; never
                                     set it in production. Warp-path shrink
                                     kernels (lora_shrink, and lora_apply's

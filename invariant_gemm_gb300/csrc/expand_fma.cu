@@ -43,11 +43,10 @@ __global__ void __launch_bounds__(kThreads, 2) expand_fma_kernel(ExpandParams p)
   uint8_t* sB = smem + 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  int64_t bid = blockIdx.x;
-  const int nt = (int)(bid % p.ntiles);
-  bid /= p.ntiles;
-  const int sl = (int)(bid % p.slices);
-  const int64_t t = bid / p.slices;
+  uint32_t bid = blockIdx.x;
+  const int nt = (int)next_digit(bid, (uint32_t)p.ntiles);
+  const int sl = (int)next_digit(bid, (uint32_t)p.slices);
+  const int64_t t = bid;
 
   // Tile entry [g, nrows, consecutive, 0, rows[8]]; complete before this kernel began.
   const int32_t* ent = p.tiles + t * kTileInts;

@@ -106,11 +106,10 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* s_zb = smem + off_zb();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int64_t bid = blockIdx.x;
-  const int nt = (int)(bid % p.ntiles);
-  bid /= p.ntiles;
-  const int sl = (int)(bid % p.slices);
-  const int64_t t = bid / p.slices;
+  uint32_t bid = blockIdx.x;
+  const int nt = (int)next_digit(bid, (uint32_t)p.ntiles);
+  const int sl = (int)next_digit(bid, (uint32_t)p.slices);
+  const int64_t t = bid;
 
   for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
   if (tid == 0) {

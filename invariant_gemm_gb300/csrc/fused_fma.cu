@@ -62,7 +62,7 @@ __host__ __device__ inline FusedLayout fused_layout(int64_t Ks, int64_t N, int S
   FusedLayout L;
   const int nkb = (int)((Ks + kShrinkKB - 1) / kShrinkKB);
   L.nst = nkb < kShrinkStages ? nkb : kShrinkStages;
-  L.cols = (int)(((N + S - 1) / S + 7) / 8 * 8);
+  L.cols = (((int)N + S - 1) / S + 7) / 8 * 8;   // N < 2^31: 32-bit division
   L.units = L.cols / F::CU;
   L.box_rows = L.units < 256 ? L.units : 256;
   L.nbox = (L.units + L.box_rows - 1) / L.box_rows;
@@ -96,9 +96,9 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
   const int s = (int)cluster_rank();
-  const int64_t cl = blockIdx.x / S;
-  const int sl = (int)(cl % p.slices);
-  const int64_t t = cl / p.slices;
+  uint32_t cl = blockIdx.x / (uint32_t)S;
+  const int sl = (int)next_digit(cl, (uint32_t)p.slices);
+  const int64_t t = cl;
 
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];
   if (tid == 0) {

@@ -267,6 +267,17 @@ __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Next digit of a block index, in 32-bit unsigned arithmetic (grids stay
+// below 2^31 blocks, and the divisors are small): v becomes v / d, the
+// remainder is returned. A 64-bit division by a runtime value costs every
+// thread a long instruction sequence; this one a few instructions.
+__device__ __forceinline__ uint32_t next_digit(uint32_t& v, uint32_t d) {
+  const uint32_t q = v / d;
+  const uint32_t rem = v - q * d;
+  v = q;
+  return rem;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

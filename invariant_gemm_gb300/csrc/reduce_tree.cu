@@ -35,11 +35,10 @@ __global__ void __launch_bounds__(kThreads) reduce_tree_kernel(TreeParams p) {
   // the next kernel may be scheduled now: it reads nothing of ours before
   // its own griddep_wait(), which waits for this grid to complete
   griddep_launch();
-  int64_t bid = blockIdx.x;
-  const int jb = (int)(bid % p.jblocks);
-  bid /= p.jblocks;
-  const int sl = (int)(bid % p.slices);
-  const int64_t t = bid / p.slices;
+  uint32_t bid = blockIdx.x;
+  const int jb = (int)next_digit(bid, (uint32_t)p.jblocks);
+  const int sl = (int)next_digit(bid, (uint32_t)p.slices);
+  const int64_t t = bid;
   const int ents = 4 + p.tile_rows;
   const int32_t* ent = p.tiles + t * ents;
   const int g = ent[0];

@@ -57,13 +57,11 @@ __global__ void __launch_bounds__(FmaGeo<BN>::THREADS)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
 
-  int64_t bid = blockIdx.x;
-  const int s = (int)(bid % S);
-  bid /= S;
-  const int jb = (int)(bid % p.jblocks);
-  bid /= p.jblocks;
-  const int sl = (int)(bid % p.slices);
-  const int64_t t = bid / p.slices;
+  uint32_t bid = blockIdx.x;
+  const int s = (int)next_digit(bid, (uint32_t)S);
+  const int jb = (int)next_digit(bid, (uint32_t)p.jblocks);
+  const int sl = (int)next_digit(bid, (uint32_t)p.slices);
+  const int64_t t = bid;
 
   // Tile entry: [g, nrows, consecutive, 0, rows[8]]; complete before this kernel began.
   if (tid < kTileInts) ent_s[tid] = p.tiles[t * kTileInts + tid];

@@ -113,12 +113,11 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
   const int ngroups = p.slices / ns;
-  int64_t bid = blockIdx.x;
-  const int s = (int)(bid % S);
-  bid /= S;
-  const int sg = (int)(bid % ngroups);
+  uint32_t bid = blockIdx.x;
+  const int s = (int)next_digit(bid, (uint32_t)S);
+  const int sg = (int)next_digit(bid, (uint32_t)ngroups);
   const int sl0 = sg * ns;
-  const int64_t t = bid / ngroups;
+  const int64_t t = bid;
   // z address of accumulator column c (four columns never straddle a slice:
   // r is a multiple of 16)
   auto zrow = [&](int c, int tok) -> float* {

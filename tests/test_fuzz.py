@@ -1,8 +1,10 @@
 """Seeded random shapes through lora_apply against the FP64 oracle: every mode
 and path on ragged sizes (M, K, N, r, slices, adapters, Split-K, share of
-tokens without an adapter), so that the hand-picked cases of the other files
-are not the only ones that hold. Deterministic modes are also replayed once
-and must give the same bits."""
+tokens without an adapter), with and without the static-weights and
+input-ready flags (copies and, in the fused decode kernel, the shrink issued
+before the dependency wait), so that the hand-picked cases of the other
+files are not the only ones that hold. Deterministic modes are also replayed
+once and must give the same bits."""
 import numpy as np
 import pytest
 import torch
@@ -34,8 +36,9 @@ def draw(i):
     L = int(rng.integers(1, 11))
     none_frac = float(rng.choice([0.0, 0.0, 0.15, 0.5]))
     ids = str(rng.choice(["uniform", "segments", "zipf"]))
+    flags = [0, ig.FLAG_STATIC_WEIGHTS, ig.FLAG_STATIC_WEIGHTS | ig.FLAG_INPUT_READY][i % 3]
     return dict(M=M, K=K, N=N, r=r, slices=slices, L=L, S=S, mode=mode, path=path,
-                none_frac=none_frac, ids=ids, seed=9100 + i)
+                none_frac=none_frac, ids=ids, seed=9100 + i, flags=flags)
 
 
 CASES = [draw(i) for i in range(36)]
@@ -46,8 +49,9 @@ def _gpu():
     need_gpu()
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "M%d_K%d_N%d_r%d_sl%d_L%d_S%d_m%d_p%d" % (
-    c["M"], c["K"], c["N"], c["r"], c["slices"], c["L"], c["S"], c["mode"], c["path"]))
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "M%d_K%d_N%d_r%d_sl%d_L%d_S%d_m%d_p%d_f%d" % (
+    c["M"], c["K"], c["N"], c["r"], c["slices"], c["L"], c["S"], c["mode"], c["path"],
+    c["flags"]))
 def test_random_shapes_against_oracle(case):
     c = case
     L = c["L"] if c["ids"] != "zipf" else max(c["L"], 2)
@@ -55,7 +59,7 @@ def test_random_shapes_against_oracle(case):
                            ids=c["ids"], segment=64, seed=c["seed"],
                            none_frac=c["none_frac"], device="cuda")
     sh = ig.make_shape(c["M"], c["K"], c["N"], c["r"], slices=c["slices"], num_adapters=L,
-                       split_k=c["S"], mode=c["mode"], path=c["path"])
+                       split_k=c["S"], mode=c["mode"], path=c["path"], flags=c["flags"])
     z, y = run_apply(p, shape=sh)
     if c["M"] == 0:
         return
