@@ -187,14 +187,18 @@ __global__ void __launch_bounds__(kThreads)
     uint8_t* st = ring + (b % nst) * stage_bytes;
     tma_load_2d(st + kXTileBytes, &p.tm_a, k0 + b * kKStep, a_row, &ctl->full[b % nst]);
   };
+  // x of k-step b: lane 0 copies the box of a tile of consecutive tokens;
+  // the rows of a scattered tile are gathered four at a time, the gathers
+  // spread over the producer warp's lanes (one thread issuing all of them
+  // held a scattered-token shrink at about 40% of the copy bandwidth)
   auto issue_x = [&](int b) {
     uint8_t* st = ring + (b % nst) * stage_bytes;
     if (contiguous) {
-      tma_load_2d(st, &p.tm_xt, k0 + b * kKStep, rows_s[0], &ctl->full[b % nst]);
+      if (lane == 0) tma_load_2d(st, &p.tm_xt, k0 + b * kKStep, rows_s[0], &ctl->full[b % nst]);
       return;
     }
     const int last = nrows - 1;
-    for (int q = 0; q < groups4; ++q)
+    for (int q = lane; q < groups4; q += 32)
       tma_gather4(st + q * 4 * 128, &p.tm_x, k0 + b * kKStep, rows_s[min(4 * q, last)],
                   rows_s[min(4 * q + 1, last)], rows_s[min(4 * q + 2, last)],
                   rows_s[min(4 * q + 3, last)], &ctl->full[b % nst]);
@@ -210,19 +214,29 @@ __global__ void __launch_bounds__(kThreads)
   griddep_wait();
   griddep_launch();
 
-  if (warp == 0 && lane == 0) {
-    // producer
+  if (warp == 0) {
+    // producer warp: lane 0 waits for a free stage, arms it with the stage's
+    // byte count and copies A; the x copies follow (the arming may come
+    // after a lane's gather has landed: the stage cannot complete before
+    // lane 0's arrival)
     for (int b = 0; b < nk; ++b) {
-      if (b >= first) {
-        const int st = b % nst;
-        if (!mbar_wait_bounded(&ctl->empty[st], (uint32_t)(((b / nst) - 1) & 1), p.status)) {
-          failed = true;
-          break;
+      int ok = 1;
+      if (lane == 0) {
+        if (b >= first) {
+          const int st = b % nst;
+          if (mbar_wait_bounded(&ctl->empty[st], (uint32_t)(((b / nst) - 1) & 1), p.status)) {
+            mbar_arrive_expect_tx(&ctl->full[st], stage_tx);
+            issue_a(b);
+          } else {
+            ok = 0;
+          }
+        } else if (!early_a) {
+          issue_a(b);
         }
-        mbar_arrive_expect_tx(&ctl->full[st], stage_tx);
-        issue_a(b);
-      } else if (!early_a) {
-        issue_a(b);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        failed = true;
+        break;
       }
       issue_x(b);
     }
