@@ -518,6 +518,8 @@ def prefill_bench(ig, device, reps):
                        key=lambda k: res[k]["us"])
             res["fastest_det"] = best
             if K == 8192 and M == 8192:
+                res["shrink_kernel_traffic"] = ncu_traffic(
+                    "shrink_mma.cu", "large_M8192_K8192_r128_N8192,S=4")
                 res["expand_kernel_traffic"] = ncu_traffic(
                     "expand_mma.cu", "large_M8192_K8192_r128_N8192,S=4")
             out["large"][f"K{K}_M{M}"] = res
@@ -806,6 +808,7 @@ PROFILE_CASES = {
     # name: (M, K, N, r, slices, L, adapter ids, Split-K, entry point)
     "qkv-shrink": (4096, 4096, 4096, 64, 3, 16, "segments", 8, "shrink"),
     "qkv-expand": (4096, 4096, 4096, 64, 3, 16, "segments", 8, "expand"),
+    "scattered-shrink": (8192, 8192, 8192, 128, 1, 64, "zipf", 4, "shrink"),
     "scattered-expand": (8192, 8192, 8192, 128, 1, 64, "zipf", 4, "expand"),
 }
 
