@@ -26,7 +26,7 @@ namespace ig {
 //
 // The counters sit at a fixed place whatever the shape, so one
 // ig_workspace_init makes a workspace valid for every later call that fits
-// in it: counters are only ever left at zero (Algorithm 1, line 14).
+// in it: counters are only ever left at zero (Algorithm 1: the last arriver resets its counter).
 // ---------------------------------------------------------------------------
 constexpr int64_t kMaxCounters = 65536;
 constexpr size_t kStatusBytes = 256;

@@ -52,7 +52,7 @@ def replay(p, mode, n, split_k=8):
         diff_runs += (ne > 0).to(torch.int64)
         diff_y += (y.view(torch.int16) != y0b).any().to(torch.int64)
     assert ig.check_status(ws) == 0
-    # Algorithm 1, line 14: every counter is back at zero
+    # Algorithm 1 (the last arriver resets its counter): every counter is back at zero
     counters = ws[256:256 + 4 * 65536].view(torch.int32)
     assert int(counters.abs().sum()) == 0
     return int(diff_runs), int(diff_elems) / (n * z0.numel()), int(diff_y)
