@@ -7,7 +7,7 @@
 // and sec. 6.2 / Fig. 5 (the FP32 shrink output reaches the next operation as
 // BF16, rounded to nearest).
 //
-// Block = 4 warps, work = one 128-row tile of one adapter (128-row tile
+// Block = 8 warps (two warpgroups), work = one 128-row tile of one adapter (128-row tile
 // table) x one slice x nb column blocks of 64 (2 <= nb <= 16, chosen on the
 // host so that the grid fills the GPU about three blocks per SM; it does not
 // change any result). The A operand of the MMA, the tile's Z rows rounded to bf16,
@@ -19,8 +19,9 @@
 // one of two stages, so the copies of
 // block i+2 are in flight while block i is computed; tcgen05.mma, M = 128,
 // N = 64, K = 16 per instruction, r/16 of them, FP32 into one of two TMEM
-// accumulators. Each thread then reads its row of the accumulator, adds it to
-// y in FP32 and rounds once to bf16 in shared memory; the tile goes back by
+// accumulators. Each thread then reads half a row of the accumulator (warp w:
+// rows 32 (w % 4) .., columns 32 (w / 4) ..), adds it to y in FP32 and rounds
+// once to bf16 in shared memory; the tile goes back by
 // one TMA store when it is 128 consecutive tokens, else by whole-row stores.
 //
 // Arithmetic, fixed by r: the tensor core's FP32 sum over j, then
@@ -31,14 +32,13 @@ namespace ig {
 
 namespace {
 
-constexpr int kThreads = 128;
 constexpr int kBN = kMmaExpandBN;                // output columns per column block
 constexpr int kYB = kBN / 64;                    // 64-column y boxes per column block
 constexpr int kYBox = kMmaTileRows * 128;        // one y box: 128 rows x 64 columns (16 KB)
 constexpr int kYBytes = kYB * kYBox;             // y tile of one column block
 constexpr int kBAtom = kBN * 128;                // B rows of one column block, per 64 ranks
 
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 2;
 
 struct Ctl {
   uint64_t full_b[kMaxStages];   // B copies of a stage
@@ -49,7 +49,9 @@ struct Ctl {
 };
 
 // Copy stages. Two: a third stage costs the third block per SM at r = 64,
-// which measured slower (84 us against 52.5 us on the QKV prefill shape).
+// which measured slower (84 us against 52.5 us on the QKV prefill shape),
+// and at r = 128 three to five stages leave one block per SM, 60% slower
+// (a block's epilogues, not its copies in flight, set the pace).
 __host__ __device__ inline int expand_stages(int) { return 2; }
 
 // layout (offsets from the 1024-aligned base): ctl 0, tile entry 128,
@@ -92,9 +94,13 @@ __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-template <int NS>
-__global__ void __launch_bounds__(kThreads)
+// WG warpgroups per block: one where shared memory leaves room for three
+// blocks per SM (at most 168 registers a thread), two where it leaves room
+// for two (at most 128), so that either way 12 or 16 warps share an SM.
+template <int NS, int WG>
+__global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
     expand_mma_kernel(const __grid_constant__ MmaExpandParams p) {
+  constexpr int kThreads = 128 * WG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -172,6 +178,24 @@ __global__ void __launch_bounds__(kThreads)
   // block's ncols are not read) and arrives once its copies have landed; row
   // gathers by TMA measured slower for scattered rows.
   const int64_t ld = (int64_t)p.slices * N;
+  // Row copies (scattered tokens) and row stores (any tile not stored as one
+  // box): thread t moves the 16-byte chunk t % 8 of tile rows
+  // m_k = t / 8 + 32k (k = 0..3) in every column block, so the rows' global
+  // offsets (column block 0; -1 past nrows) and the swizzled place of the
+  // chunk (the same for every k, 32k being a multiple of 8) are computed once
+  // per block.
+  static_assert(kYB == 1, "one 64-column y box per column block");
+  constexpr int kRowSets = kMmaTileRows * 8 / kThreads;   // rows per thread
+  const int ych = tid & 7;
+  const int ym = tid >> 3;
+  const uint32_t ys_off = (uint32_t)ym * 128u + ((uint32_t)(ych ^ (ym & 7)) << 4);
+  constexpr uint32_t kRowSetBytes = (kThreads / 8) * 128;
+  int64_t yoff[kRowSets];
+#pragma unroll
+  for (int k = 0; k < kRowSets; ++k) {
+    const int m = ym + (kThreads / 8) * k;
+    yoff[k] = m < nrows ? (int64_t)rows_s[m] * ld + y_col + ych * 8 : -1;
+  }
   auto issue_y = [&](int i) {   // thread 0 (consecutive tokens) or every thread
     uint8_t* sy = stage(i) + ka * kBAtom;
     if (contiguous) {
@@ -184,12 +208,11 @@ __global__ void __launch_bounds__(kThreads)
       return;
     }
     const int nc = (int)min((int64_t)kBN, N - n0 - (int64_t)i * kBN);
-    const int ch = tid & 7;
-    for (int yb = 0; yb < kYB; ++yb) {
-      if (yb * 64 + ch * 8 >= nc) continue;
-      for (int m = tid >> 3; m < nrows; m += kThreads / 8)
-        cp_async16(sy + yb * kYBox + m * 128 + ((ch ^ (m & 7)) << 4),
-                   p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + yb * 64 + ch * 8);
+    if (ych * 8 < nc) {
+      const __nv_bfloat16* yi = p.y + (int64_t)i * kBN;
+#pragma unroll
+      for (int k = 0; k < kRowSets; ++k)
+        if (yoff[k] >= 0) cp_async16(sy + ys_off + kRowSetBytes * k, yi + yoff[k]);
     }
     cp_async_mbar_arrive(&ctl->full_y[i % NS]);
   };
@@ -212,14 +235,15 @@ __global__ void __launch_bounds__(kThreads)
   // mid = bf16_rn(z - hi) and lo = bf16_rn(z - hi - mid) (hi + mid + lo == z
   // exactly), in atoms after the hi ones.
   {
+    constexpr int kWRows = kMmaTileRows / (kThreads / 32);   // rows per warp
     const int per_row = r / 4;
-    const int total = 32 * per_row;           // float4 of the warp's 32 rows
+    const int total = kWRows * per_row;       // float4 of the warp's rows
     for (int b0 = 0; b0 < total; b0 += 16 * 32) {
       float4 f4[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int idx = b0 + lane + 32 * k;
-        const int m = warp * 32 + idx / per_row;
+        const int m = warp * kWRows + idx / per_row;
         f4[k] = idx < total && m < nrows
                     ? __ldcg(reinterpret_cast<const float4*>(
                           p.z + ((int64_t)sl * M + rows_s[m]) * r + 4 * (idx % per_row)))
@@ -229,7 +253,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int k = 0; k < 16; ++k) {
         const int idx = b0 + lane + 32 * k;
         if (idx >= total) continue;
-        const int m = warp * 32 + idx / per_row;
+        const int m = warp * kWRows + idx / per_row;
         const int j = 4 * (idx % per_row);
         const float fv[4] = {f4[k].x, f4[k].y, f4[k].z, f4[k].w};
         uint32_t pt[3][4];   // bf16 parts hi, mid, lo
@@ -308,19 +332,20 @@ __global__ void __launch_bounds__(kThreads)
     const bool mine = y_ok && acc_ok;
     uint8_t* sy = stage(i) + ka * kBAtom;
 
-    // epilogue 1: this thread's row: y = bf16_rn(f32(y) + acc), in shared memory
-    {
-      const int m = tid;
-      const uint32_t trow = tmem + (uint32_t)((i & 1) * kBN) + ((uint32_t)(warp * 32) << 16);
-#pragma unroll
-      for (int c = 0; c < kBN; c += 32) {
-        float v[32];
-        tmem_ld32(trow + c, v);
-        if (m >= nrows || !mine) continue;
-        uint8_t* rowp = sy + (c / 64) * kYBox + m * 128;
+    // epilogue 1: y = bf16_rn(f32(y) + acc), in shared memory. Warp w reads
+    // accumulator rows 32 (w % 4) .. + 31 (the lanes of tensor memory it may
+    // access); warpgroup g the 32-column halves g, g + WG, ... of them
+    const int m = 32 * (warp & 3) + lane;
+    const uint32_t trow = tmem + (uint32_t)((i & 1) * kBN) + ((uint32_t)(32 * (warp & 3)) << 16);
+    static_assert(kBN == 64, "two 32-column halves per column block");
+    for (int c = 32 * (warp >> 2); c < kBN; c += 32 * WG) {
+      float v[32];
+      tmem_ld32(trow + c, v);
+      if (m < nrows && mine) {
+        uint8_t* rowp = sy + m * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int chunk = (c % 64) / 8 + q;                // logical 16-byte chunk
+          const int chunk = c / 8 + q;                       // logical 16-byte chunk
           uint4* cp = reinterpret_cast<uint4*>(rowp + ((chunk ^ (m & 7)) * 16));
           uint4 u = *cp;
           float yf[8];
@@ -354,17 +379,16 @@ __global__ void __launch_bounds__(kThreads)
         bulk_commit();
       }
     } else {
-      // four rows (128 bytes of one 64-column box each) per warp-instruction
-      for (int yb = 0; yb < kYB; ++yb)
-        for (int m0 = 4 * warp; m0 < nrows; m0 += 16) {
-          const int m = m0 + lane / 8;
-          const int ch = lane % 8;              // 16-byte chunk of the 128-byte row
-          if (m >= nrows || yb * 64 + ch * 8 >= ncols) continue;
-          const uint4 u = *reinterpret_cast<const uint4*>(sy + yb * kYBox + m * 128 +
-                                                          ((ch ^ (m & 7)) * 16));
-          *reinterpret_cast<uint4*>(p.y + (int64_t)rows_s[m] * ld + y_col + i * kBN + yb * 64 +
-                                    ch * 8) = u;
-        }
+      // four rows (128 bytes each) per warp-instruction, the rows and chunk
+      // of the scattered-token copies above
+      if (ych * 8 < ncols) {
+        __nv_bfloat16* yi = p.y + (int64_t)i * kBN;
+#pragma unroll
+        for (int k = 0; k < kRowSets; ++k)
+          if (yoff[k] >= 0)
+            *reinterpret_cast<uint4*>(yi + yoff[k]) =
+                *reinterpret_cast<const uint4*>(sy + ys_off + kRowSetBytes * k);
+      }
       __syncthreads();
     }
     // stage i % NS is free once the store has read it: copies of block i + NS
@@ -398,14 +422,21 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_expand_mma(const MmaExpandParams& p, int64_t tiles_max, cudaStream_t st) {
   const size_t smem = mma_expand_smem((int)p.r, (p.flags & IG_FLAG_Z_FP32) != 0);
-  void (*kern)(MmaExpandParams) =
-        expand_stages((int)p.r) == 3 ? expand_mma_kernel<3> : expand_mma_kernel<2>;
+  // shared memory of one SM; each resident block also takes 1 KB of it
+  static const int sm_smem = [] {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    return v;
+  }();
+  const int wg = 3 * (smem + 1024) <= (size_t)sm_smem ? 1 : 2;
+  void (*kern)(MmaExpandParams) = wg == 1 ? expand_mma_kernel<2, 1> : expand_mma_kernel<2, 2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = tiles_max * p.slices * p.ntiles;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(128 * wg), smem, st, p);
 }
 
 size_t expand_mma_smem_bytes(int r, bool z_fp32) { return mma_expand_smem(r, z_fp32); }
