@@ -189,8 +189,10 @@ __global__ void __launch_bounds__(kThreads)
   };
   // x of k-step b: lane 0 copies the box of a tile of consecutive tokens;
   // the rows of a scattered tile are gathered four at a time, the gathers
-  // spread over the producer warp's lanes (one thread issuing all of them
-  // held a scattered-token shrink at about 40% of the copy bandwidth)
+  // spread over the 32 lanes of a warp, warp 0 for the even k-steps and
+  // warp 2 for the odd ones (one thread issuing all of them held a
+  // scattered-token shrink at 40% of the copy bandwidth, one warp at 49%,
+  // two warps at 58%, three warps at 55%)
   auto issue_x = [&](int b) {
     uint8_t* st = ring + (b % nst) * stage_bytes;
     if (contiguous) {
@@ -234,6 +236,19 @@ __global__ void __launch_bounds__(kThreads)
           issue_a(b);
         }
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        failed = true;
+        break;
+      }
+      if (contiguous || (b & 1) == 0) issue_x(b);
+    }
+  } else if (warp == 2 && !contiguous) {
+    // second gather warp of a scattered tile: the x rows of the odd k-steps,
+    // once their stage is free (lane 0 of warp 0 arms it)
+    for (int b = 1; b < nk; b += 2) {
+      int ok = 1;
+      if (lane == 0 && b >= first)
+        ok = mbar_wait_bounded(&ctl->empty[b % nst], (uint32_t)(((b / nst) - 1) & 1), p.status);
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
         failed = true;
         break;
