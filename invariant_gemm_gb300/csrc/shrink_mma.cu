@@ -27,20 +27,21 @@
 // through distributed shared memory measured slower: 84 KB per block at the
 // QKV shape took 7.8 us against 4.8 us through L2.)
 //
-// Block = 4 warps, tile = up to 128 token rows of one adapter (one entry of
+// Block = 8 warps, tile = up to 128 token rows of one adapter (one entry of
 // the token map's 128-row tile table) x all r rank columns of one slice, or of
 // all slices at once where slices x r <= 256 (the slices' A rows are
 // consecutive in A_stack, so one tiled copy and one MMA of N = slices x r
-// serve them, and the x tile is read once instead of once per slice). One thread of
-// warp 0 issues the TMA copies: per k-step of 64 elements, x as one 128-row
-// box when the tile's tokens are consecutive (else row gathers, 4 rows each,
-// only the tile's rows) and one tiled copy of the A block (r rows), all
-// 128-byte swizzled, into a 4-deep ring. One thread of warp 1
-// issues per k-step four tcgen05.mma (M = 128 tokens, N = r, K = 16) into an
-// FP32 accumulator in tensor memory and commits each stage back to the
-// producer. The last k-step of a partition that is not a multiple of 64
-// issues only the MMAs inside the partition. All 4 warps then read the
-// accumulator (warp w: token rows 32w .. 32w+31, one row per thread).
+// serve them, and the x tile is read once instead of once per slice). Warp 0
+// issues the TMA copies: per k-step of 64 elements, x as one 128-row box
+// when the tile's tokens are consecutive (else row gathers, 4 rows each,
+// only the tile's rows, from the lanes of warps 0 and 2) and one tiled copy
+// of the A block (r rows), all 128-byte swizzled, into a 2- to 4-deep ring.
+// One thread of warp 1 issues per k-step four tcgen05.mma (M = 128 tokens,
+// N = r, K = 16) into an FP32 accumulator in tensor memory and commits each
+// stage back to the producer. The last k-step of a partition that is not a
+// multiple of 64 issues only the MMAs inside the partition. All 8 warps then
+// read the accumulator (warp w: token rows 32 (w % 4) .. + 31, one row per
+// thread, every other 32 columns from column 32 (w / 4)).
 //
 // Arithmetic order, fixed by K/S and r only: the tensor core's FP32
 // accumulation of the K-steps in order within the partition, then the
@@ -56,7 +57,7 @@ namespace ig {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // two warpgroups: both read the accumulator
 constexpr int kMaxStages = 4;
 // Copy ring depth: 4 stages up to r = 64, 3 at r = 128, 2 at r = 256, so that
 // two blocks share an SM (one per SM leaves 16-block clusters short of SMs).
@@ -281,8 +282,11 @@ __global__ void __launch_bounds__(kThreads)
   // epilogue: wait for the accumulator
   const bool acc_ok = mbar_wait_bounded(&ctl->done, 0, p.status);
   tc_fence_after();
-  const int row = warp * 32 + lane;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  // warp w reads accumulator rows 32 (w % 4) .. + 31 (the lanes of tensor
+  // memory it may access), warpgroup cg = w / 4 every other 32 columns
+  const int row = 32 * (warp & 3) + lane;
+  const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  const int cg = warp >> 2;
   if (CL) {
     // This block's partial -> slot s of the tile's workspace area, staged in
     // shared memory (the ring: every MMA of this block has completed) half
@@ -294,7 +298,7 @@ __global__ void __launch_bounds__(kThreads)
     const int rowf = cw + 4;                      // padded staged row, floats
     float* stg = reinterpret_cast<float*>(ring);  // [128][rowf]
     for (int h = 0; h < 2; ++h) {
-      for (int c = 0; c < cw; c += 32) {
+      for (int c = 32 * cg; c < cw; c += 64) {
         float v[32];
         tmem_ld32(trow + h * cw + c, v);
         const int nv = acc_ok ? min(32, cw - c) : 0;
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   const int64_t slot = t * ngroups + sg;
   float* part = p.partials + slot * (int64_t)S * (kMmaTileRows * nc);
-  for (int c = 0; c < nc; c += 32) {
+  for (int c = 32 * cg; c < nc; c += 64) {
     float v[32];
     tmem_ld32(trow + c, v);
     if (!acc_ok || row >= nrows) continue;
