@@ -416,10 +416,10 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     if ((uint32_t)ctl->info[0] == (uint32_t)(S - 1)) {
       __threadfence();
-      // Each thread owns up to 16 float4 outputs (four consecutive columns of
-      // one row) and adds the partitions q = 0..S-1 in order; the 16 loads of
-      // one partition are in flight together.
-      constexpr int kPer = 16;
+      // Each thread owns up to kPer float4 outputs (four consecutive columns
+      // of one row) and adds the partitions q = 0..S-1 in order; the kPer
+      // loads of one partition are in flight together (2048 per block).
+      constexpr int kPer = 2048 / kThreads;
       const int n4 = nrows * nc / 4;
       for (int base = 0; base < n4; base += kPer * kThreads) {
         float4 tot[kPer];
