@@ -210,9 +210,11 @@ const char* ig_version(void);
 const char* ig_status_string(int status);
 
 /* Bytes of device workspace a call with this shape needs: status word,
- * per-tile completion counters, the token map (rows grouped by adapter) and,
- * for IG_MODE_DET, the FP32 partials [tiles][S][BM x BN]. Returns 0 for an
- * invalid shape. Host only. */
+ * per-tile completion counters, the token map (rows grouped by adapter),
+ * for IG_MODE_DET and IG_MODE_DET_TREE the FP32 partials [tiles][S][BM x BN],
+ * and on the tcgen05 path in IG_MODE_DET and IG_MODE_UNSPLIT the expand's Z
+ * operand that the shrink of lora_apply writes (bf16 z per tile, slice and
+ * bf16 part). Returns 0 for an invalid shape. Host only. */
 size_t ig_workspace_bytes(const ig_shape* shape);
 
 /* Resolve the plan for a shape without touching the GPU. IG_OK or an

@@ -24,7 +24,7 @@ struct Plan {
   int tile_rows;     // rows per tile: 8 (warp and FMA paths) or 128 (tcgen05)
   int64_t tiles;     // tile-table entries: upper bound on tiles (groups 0..L)
   int ntiles;        // expand column tiles per slice
-  size_t off_perm, off_offsets, off_tiles, off_partials, total;
+  size_t off_perm, off_offsets, off_tiles, off_partials, off_zt, zt_bytes, total;
   bool fused;        // lora_apply runs the one-launch cluster kernel
   uint64_t key;
 };
@@ -97,7 +97,14 @@ int make_plan(const ig_shape* sh, Plan* pl) {
       align_up(pl->off_tiles + 4 * (size_t)(4 + pl->tile_rows) * pl->tiles, 256);
   size_t part = 0;
   if (partials) part = (size_t)slots * S * pl->tile_rows * pl->bn * sizeof(float);
-  pl->total = align_up(pl->off_partials + part, 256);
+  // the tcgen05 expand's Z operand, written by the shrink inside lora_apply
+  // where one block writes each final z value (DET, UNSPLIT)
+  pl->off_zt = align_up(pl->off_partials + part, 1024);
+  pl->zt_bytes = (mma && (sh->mode == IG_MODE_DET || sh->mode == IG_MODE_UNSPLIT))
+                     ? (size_t)pl->tiles * sh->slices *
+                           zt_entry_bytes(r, (sh->flags & IG_FLAG_Z_FP32) != 0)
+                     : 0;
+  pl->total = align_up(pl->off_zt + pl->zt_bytes, 256);
 
   // The fused kernel expands N/S columns per block; past 1024 the two-kernel
   // path (256-column expand blocks) is faster. Both give the same bits.
@@ -162,7 +169,7 @@ int run_map(const ig_shape* sh, const Plan& pl, const int32_t* idx, uint8_t* ws,
 }
 
 int run_shrink_mma(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
-                   float scale, float* z, uint8_t* ws, cudaStream_t st) {
+                   float scale, float* z, uint8_t* ws, cudaStream_t st, uint8_t* zt) {
   MmaShrinkParams p;
   int rc = encode_map_2d(&p.tm_x, x, (uint64_t)sh->M, (uint64_t)sh->K, (uint64_t)sh->K * 2, 64,
                          1, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -189,11 +196,12 @@ int run_shrink_mma(const ig_shape* sh, const Plan& pl, const void* x, const void
   p.stack = pl.stack;
   p.flags = sh->flags;
   p.scale = scale;
+  p.zt = zt;
   return cuda_status(launch_shrink_mma(p, pl.mode, pl.tiles, st));
 }
 
 int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
-                   uint8_t* ws, cudaStream_t st) {
+                   uint8_t* ws, cudaStream_t st, const uint8_t* zt) {
   MmaExpandParams p;
   int rc = encode_map_2d(&p.tm_b, B, (uint64_t)sh->num_adapters * sh->slices * sh->N,
                          (uint64_t)sh->r, (uint64_t)sh->r * 2, 64, kMmaExpandBN,
@@ -221,6 +229,7 @@ int run_expand_mma(const ig_shape* sh, const Plan& pl, const float* z, const voi
                                 std::max<int64_t>(2, (units + target - 1) / target));
   p.ntiles = (int)((nblk + p.nb - 1) / p.nb);
   p.flags = sh->flags;
+  p.zt = zt;
   return cuda_status(launch_expand_mma(p, pl.tiles, st));
 }
 
@@ -243,22 +252,23 @@ int run_tree(const ig_shape* sh, const Plan& pl, float scale, float* z, uint8_t*
 }
 
 int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
-                    float scale, float* z, uint8_t* ws, cudaStream_t st);
+                    float scale, float* z, uint8_t* ws, cudaStream_t st, uint8_t* zt = nullptr);
 
+// zt: where the tcgen05 shrink also writes the expand's Z operand (lora_apply)
 int run_shrink(const ig_shape* sh, const Plan& pl, const void* x, const void* A, float scale,
-               float* z, uint8_t* ws, cudaStream_t st) {
-  const int rc = run_shrink_only(sh, pl, x, A, scale, z, ws, st);
+               float* z, uint8_t* ws, cudaStream_t st, uint8_t* zt = nullptr) {
+  const int rc = run_shrink_only(sh, pl, x, A, scale, z, ws, st, zt);
   if (rc != IG_OK || pl.mode != IG_MODE_DET_TREE) return rc;
   return run_tree(sh, pl, scale, z, ws, st);
 }
 
 int run_shrink_only(const ig_shape* sh, const Plan& pl, const void* x, const void* A,
-                    float scale, float* z, uint8_t* ws, cudaStream_t st) {
+                    float scale, float* z, uint8_t* ws, cudaStream_t st, uint8_t* zt) {
   if (pl.mode == IG_MODE_ATOMIC) {
     cudaError_t e = cudaMemsetAsync(z, 0, sizeof(float) * sh->slices * sh->M * sh->r, st);
     if (e != cudaSuccess) return IG_ERR_CUDA;
   }
-  if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st);
+  if (pl.path == IG_PATH_MMA) return run_shrink_mma(sh, pl, x, A, scale, z, ws, st, zt);
   ShrinkParams p;
   const bool fma = pl.path == IG_PATH_FMA;
   // x (FMA path only; the warp path loads x into registers): 256-element
@@ -352,9 +362,10 @@ int run_fused(const ig_shape* sh, const Plan& pl, const void* x, const void* A, 
   return cuda_status(launch_fused_warp(p, pl.bn, pl.tiles, st));
 }
 
+// zt: the Z operand the shrink wrote (lora_apply), or null: built from z
 int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B, void* y,
-               uint8_t* ws, cudaStream_t st) {
-  if (pl.path == IG_PATH_MMA) return run_expand_mma(sh, pl, z, B, y, ws, st);
+               uint8_t* ws, cudaStream_t st, const uint8_t* zt = nullptr) {
+  if (pl.path == IG_PATH_MMA) return run_expand_mma(sh, pl, z, B, y, ws, st, zt);
   ExpandParams p;
   if (pl.path != IG_PATH_FMA) {   // the FMA expand copies B with 1-D bulk copies
     int rc = encode_map_2d(&p.tm_b, B,
@@ -518,9 +529,10 @@ int lora_apply(const ig_shape* shape, const void* x, void* y, const int32_t* ada
     if (rc != IG_OK) return rc;
   }
   if (pl.fused) return run_fused(shape, pl, x, A_stack, B_stack, scale, z, y, w, st);
-  rc = run_shrink(shape, pl, x, A_stack, scale, z, w, st);
+  uint8_t* zt = pl.zt_bytes ? w + pl.off_zt : nullptr;
+  rc = run_shrink(shape, pl, x, A_stack, scale, z, w, st, zt);
   if (rc != IG_OK) return rc;
-  return run_expand(shape, pl, z, B_stack, y, w, st);
+  return run_expand(shape, pl, z, B_stack, y, w, st, zt);
 }
 
 int ig_check_status(void* ws, size_t ws_bytes, void* stream) {

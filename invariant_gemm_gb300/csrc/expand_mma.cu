@@ -44,6 +44,7 @@ struct Ctl {
   uint64_t full_b[kMaxStages];   // B copies of a stage
   uint64_t full_y[kMaxStages];   // y copies of a stage
   uint64_t done[2];              // MMAs of an accumulator
+  uint64_t zbar;                 // the Z operand copy (Z written by the shrink)
   uint32_t tmem;
   int32_t fail;                  // a B copy never arrived
 };
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
       mbar_init(&ctl->full_y[i], contig ? 1 : kThreads);
     }
     for (int i = 0; i < 2; ++i) mbar_init(&ctl->done[i], 1);
+    mbar_init(&ctl->zbar, 1);
     ctl->fail = 0;
     fence_mbar_init();
   }
@@ -221,6 +223,14 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
     for (int i = 0; i < min(nb, NS); ++i) issue_b(i);
   griddep_wait();
   griddep_launch();
+  // Z written by the shrink as this tile's operand: one bulk copy per atom,
+  // ahead of the y copies
+  const uint32_t zt_bytes = (uint32_t)zt_entry_bytes(r, zf32);
+  if (p.zt && tid == 0) {
+    const uint8_t* src = p.zt + ((size_t)t * p.slices + sl) * zt_bytes;
+    mbar_arrive_expect_tx(&ctl->zbar, zt_bytes);
+    for (uint32_t o = 0; o < zt_bytes; o += 16384) bulk_g2s(s_zb + o, src + o, 16384, &ctl->zbar);
+  }
   for (int i = 0; i < min(nb, NS); ++i) {
     if (tid == 0 && !early_b) issue_b(i);
     issue_y(i);
@@ -234,7 +244,10 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
   // added up to most of the block's life). With FP32 Z also
   // mid = bf16_rn(z - hi) and lo = bf16_rn(z - hi - mid) (hi + mid + lo == z
   // exactly), in atoms after the hi ones.
-  {
+  if (p.zt) {
+    // a copy that never lands fails the block's first accumulator wait
+    if (!mbar_wait_bounded(&ctl->zbar, 0, p.status)) ctl->fail = 1;
+  } else {
     constexpr int kWRows = kMmaTileRows / (kThreads / 32);   // rows per warp
     const int per_row = r / 4;
     const int total = kWRows * per_row;       // float4 of the warp's rows
@@ -414,6 +427,7 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
     if (tid == 32)
       for (int b = i; b < next_mma; ++b)
         mbar_wait_bounded(&ctl->done[b & 1], (uint32_t)((b >> 1) & 1), p.status);
+    if (tid == 0 && p.zt) mbar_wait_bounded(&ctl->zbar, 0, p.status);
   }
   teardown();
 }

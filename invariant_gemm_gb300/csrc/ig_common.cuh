@@ -54,6 +54,14 @@ constexpr int kExpandBN = 256;        // output columns per expand block: 4 warp
 constexpr int kArithRevision = 4;
 // tensor-core path: 128-row tiles (the MMA's M)
 constexpr int kMmaTileRows = 128;
+// Z operand of the tcgen05 expand for one (tile, slice): the tile's 128 rows
+// of Z as bf16 (three parts hi, mid, lo with FP32 Z), each part ceil(r / 64)
+// atoms of [128 rows][128 bytes], 128-byte swizzled (16-byte chunk c of row m
+// at chunk c ^ (m % 8)). Written by the shrink inside lora_apply, so that the
+// expand copies it instead of building it from z.
+__host__ __device__ inline size_t zt_entry_bytes(int64_t r, bool z_fp32) {
+  return (size_t)((r + 63) / 64) * 16384u * (z_fp32 ? 3u : 1u);
+}
 constexpr int kMmaTileInts = 4 + kMmaTileRows;
 constexpr int kMmaExpandCols = 1024;   // most output columns per tensor-core expand block
 constexpr int kMmaExpandBN = 64;       // output columns per MMA (N) of that block
@@ -151,6 +159,7 @@ struct MmaShrinkParams {
   int32_t slices, L, S, flags;
   int32_t stack;        // slices per block (1, or all slices: MMA N = slices x r)
   float scale;
+  uint8_t* zt;          // Z operand tiles for the expand (entry t * slices + slice), or null
 };
 
 struct MmaExpandParams {
@@ -163,6 +172,7 @@ struct MmaExpandParams {
   int64_t M, N, r;
   int32_t slices, L, ntiles, flags;
   int32_t nb;           // 64-column blocks per thread block (columns per block / 64)
+  const uint8_t* zt;    // Z operand tiles written by the shrink, or null: build from z
 };
 
 struct TreeParams {

@@ -96,6 +96,43 @@ __host__ __device__ inline uint32_t tmem_cols_for(int r) {
   return c;
 }
 
+// The expand's Z operand (zt_entry_bytes layout): ranks j .. j+3 (j % 4 == 0)
+// of tile row m, bf16 parts of the final z values as the expand would round
+// or split them.
+__device__ __forceinline__ void zt_put4(uint8_t* ent, int ka, bool zf32, int m, int j,
+                                        float4 zv) {
+  const float f[4] = {zv.x, zv.y, zv.z, zv.w};
+  uint32_t pt[3][4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint16_t h, md, l;
+    split_z(f[e], zf32, h, md, l);
+    pt[0][e] = h;
+    pt[1][e] = md;
+    pt[2][e] = l;
+  }
+  const size_t off = (size_t)(j / 64) * 16384 + (size_t)m * 128 +
+                     ((((j % 64) / 8) ^ (m & 7)) << 4) + (j % 8) * 2;
+  for (int q = 0; q < (zf32 ? 3 : 1); ++q)
+    *reinterpret_cast<uint2*>(ent + (size_t)q * ka * 16384 + off) =
+        make_uint2(pt[q][0] | (pt[q][1] << 16), pt[q][2] | (pt[q][3] << 16));
+}
+
+// Zero, in every part, the 16-byte chunks of tile rows [m0, m1) from rank
+// column cfrom on (a multiple of 8): rows past the tile's tokens (cfrom = 0)
+// and the ranks past r in the last atom, which the expand's MMAs read.
+__device__ __forceinline__ void zt_zero(uint8_t* ent, int ka, int parts, int m0, int m1,
+                                        int cfrom, int tid, int nthr) {
+  const int c0 = cfrom / 8, nch = ka * 8 - c0, nr = m1 - m0;
+  if (nch <= 0 || nr <= 0) return;
+  for (int i = tid; i < parts * nr * nch; i += nthr) {
+    const int q = i / (nr * nch), rem = i % (nr * nch);
+    const int m = m0 + rem / nch, cc = c0 + rem % nch;
+    *reinterpret_cast<uint4*>(ent + (size_t)(q * ka + cc / 8) * 16384 + (size_t)m * 128 +
+                              (((cc % 8) ^ (m & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // CL (IG_MODE_DET only): the S partition blocks of a tile are one cluster and
 // combine there instead of through scratch and the counter.
 template <int MODE, bool CL>
@@ -127,6 +164,13 @@ __global__ void __launch_bounds__(kThreads)
   auto zrow = [&](int c, int tok) -> float* {
     return p.z + ((int64_t)(sl0 + c / r) * p.M + tok) * r + c % r;
   };
+  // the expand's Z operand (lora_apply): entry of slice sl0 + c / r
+  const bool zf32 = (p.flags & IG_FLAG_Z_FP32) != 0;
+  const int zka = (r + 63) / 64;
+  const size_t zt_bytes = zt_entry_bytes(r, zf32);
+  auto zt_ent = [&](int sl) -> uint8_t* {
+    return p.zt + ((size_t)t * p.slices + sl) * zt_bytes;
+  };
 
   for (int i = tid; i < kMmaTileInts; i += kThreads) ent_s[i] = p.tiles[t * kMmaTileInts + i];
   if (tid == 0) {
@@ -153,6 +197,14 @@ __global__ void __launch_bounds__(kThreads)
   // receives the S partials of its valid rows
   const int R = kMmaTileRows / S;
   const int own_rows = max(0, min(R, nrows - s * R));
+  // zero the rows [m0, m1) past nrows and the ranks past r of rows
+  // [m0, min(m1, nrows)) in the block's slices
+  auto zt_pad = [&](int m0, int m1) {
+    for (int k = 0; k < ns; ++k) {
+      zt_zero(zt_ent(sl0 + k), zka, zf32 ? 3 : 1, max(m0, nrows), m1, 0, tid, kThreads);
+      if (r % 64) zt_zero(zt_ent(sl0 + k), zka, zf32 ? 3 : 1, m0, min(m1, nrows), r, tid, kThreads);
+    }
+  };
 
   auto teardown = [&]() {
     tc_fence_before();
@@ -354,11 +406,13 @@ __global__ void __launch_bounds__(kThreads)
           }
         }
         const int o = 4 * o4;
-        *reinterpret_cast<float4*>(zrow(o % nc, rows_s[s * R + o / nc])) =
-            make_float4(total.x * p.scale, total.y * p.scale, total.z * p.scale,
-                        total.w * p.scale);
+        const float4 zv = make_float4(total.x * p.scale, total.y * p.scale,
+                                      total.z * p.scale, total.w * p.scale);
+        *reinterpret_cast<float4*>(zrow(o % nc, rows_s[s * R + o / nc])) = zv;
+        if (p.zt) zt_put4(zt_ent(sl0 + (o % nc) / r), zka, zf32, s * R + o / nc, (o % nc) % r, zv);
       }
     }
+    if (p.zt && acc_ok) zt_pad(s * R, s * R + R);
     // The owned rows' partial lines are read and dead (the next call writes
     // them again before reading them): drop them from L2 without writing them
     // back. Each owner's R rows of a slot are whole 128-byte lines.
@@ -394,10 +448,12 @@ __global__ void __launch_bounds__(kThreads)
     } else if (MODE == IG_MODE_UNSPLIT) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (4 * i < nv)
-          *reinterpret_cast<float4*>(zrow(c + 4 * i, rows_s[row])) =
-              make_float4(v[4 * i] * p.scale, v[4 * i + 1] * p.scale, v[4 * i + 2] * p.scale,
-                          v[4 * i + 3] * p.scale);
+        if (4 * i < nv) {
+          const float4 zv = make_float4(v[4 * i] * p.scale, v[4 * i + 1] * p.scale,
+                                        v[4 * i + 2] * p.scale, v[4 * i + 3] * p.scale);
+          *reinterpret_cast<float4*>(zrow(c + 4 * i, rows_s[row])) = zv;
+          if (p.zt) zt_put4(zt_ent(sl0 + (c + 4 * i) / r), zka, zf32, row, (c + 4 * i) % r, zv);
+        }
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -405,6 +461,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 
+  if (MODE == IG_MODE_UNSPLIT && p.zt && acc_ok) zt_pad(0, kMmaTileRows);
   if (MODE == IG_MODE_DET) {
     __threadfence();
     __syncthreads();
@@ -447,11 +504,13 @@ __global__ void __launch_bounds__(kThreads)
           const int o4 = base + i * kThreads + tid;
           if (o4 >= n4) continue;
           const int o = 4 * o4;
-          *reinterpret_cast<float4*>(zrow(o % nc, rows_s[o / nc])) =
-              make_float4(tot[i].x * p.scale, tot[i].y * p.scale, tot[i].z * p.scale,
-                          tot[i].w * p.scale);
+          const float4 zv = make_float4(tot[i].x * p.scale, tot[i].y * p.scale,
+                                        tot[i].z * p.scale, tot[i].w * p.scale);
+          *reinterpret_cast<float4*>(zrow(o % nc, rows_s[o / nc])) = zv;
+          if (p.zt) zt_put4(zt_ent(sl0 + (o % nc) / r), zka, zf32, o / nc, (o % nc) % r, zv);
         }
       }
+      if (p.zt) zt_pad(0, kMmaTileRows);
       if (tid == 0) p.counters[slot] = 0u;
     }
   }

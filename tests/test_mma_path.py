@@ -81,16 +81,18 @@ def test_mma_replay_bitwise():
 
 
 @pytest.mark.parametrize("mode", MODES, ids=MODE_ID.get)
-def test_mma_contiguous_tiles_with_overhang(mode):
+@pytest.mark.parametrize("r", [64, 128])
+def test_mma_contiguous_tiles_with_overhang(mode, r):
     """Tiles whose tokens are consecutive are copied as one 128-row box; the
-    last tile of a single-adapter batch of 300 rows reaches past row M."""
-    p = synth.make_problem(300, 4096, 520, 64, slices=2, L=1, ids="single", seed=77,
+    last tile of a single-adapter batch of 300 rows reaches past row M (its
+    rows go back by row stores; at r = 128 the expand runs two warpgroups)."""
+    p = synth.make_problem(300, 4096, 520, r, slices=2, L=1, ids="single", seed=77,
                            device="cuda")
     z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
     check_shrink(p.to("cpu"), z)
     check_expand(p.to("cpu"), z, y)
     # segments of 256 tokens per adapter (the prefill layout) with a ragged end
-    p = synth.make_problem(700, 4096, 512, 64, L=3, ids="segments", segment=256, seed=78,
+    p = synth.make_problem(700, 4096, 512, r, L=3, ids="segments", segment=256, seed=78,
                            device="cuda")
     z, y = run_apply(p, mode=mode, path=ig.PATH_MMA)
     check_shrink(p.to("cpu"), z)
@@ -113,3 +115,32 @@ def test_mma_cluster_combine_bitwise_equals_counter(r, K, S):
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
     check_shrink(p.to("cpu"), outs[0][0])
     check_expand(p.to("cpu"), outs[0][0], outs[0][1])
+
+
+@pytest.mark.parametrize("mode,flags", [(ig.MODE_DET, 0), (ig.MODE_DET, ig.FLAG_UNFUSED),
+                                        (ig.MODE_UNSPLIT, 0), (ig.MODE_DET, ig.FLAG_Z_FP32)],
+                         ids=["det_cluster", "det_counter", "unsplit", "det_z_fp32"])
+@pytest.mark.parametrize("r,slices", [(32, 3), (48, 2), (128, 1), (192, 1)])
+def test_apply_z_operand_equals_separate_calls(mode, flags, r, slices):
+    """Inside lora_apply the tcgen05 shrink also writes the expand's Z operand
+    (bf16 tiles in the tensor cores' layout) and the expand copies it instead
+    of building it from z; lora_shrink then lora_expand build it from z. Same
+    rounding of the same z values, so the same bits, on scattered and
+    consecutive tiles, partly filled tiles and ranks that end inside an
+    atom (r = 48, 192)."""
+    for ids, seed in (("uniform", 11), ("segments", 12)):
+        p = synth.make_problem(333, 4096, 520, r, slices=slices, L=5, ids=ids, segment=96,
+                               seed=seed + r, none_frac=0.1, device="cuda")
+        sh = ig.make_shape(p.M, p.K, p.N, r, slices=slices, num_adapters=5, split_k=8,
+                           mode=mode, path=ig.PATH_MMA, flags=flags)
+        z1, y1 = run_apply(p, shape=sh)
+        ws = ig.workspace(sh)
+        z2 = torch.full_like(z1, float("nan"))
+        y2 = p.y.clone()
+        ig.lora_shrink(sh, p.x, p.A, p.idx, p.scale, z2, ws)
+        ig.lora_expand(sh, z2, p.B, p.idx, y2, ws)
+        assert ig.check_status(ws) == 0
+        assert torch.equal(z1.view(torch.int32), z2.view(torch.int32))
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+        if not flags & ig.FLAG_Z_FP32:
+            check_expand(p.to("cpu"), z1, y1)
