@@ -221,10 +221,17 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
 
   if (tid == 0 && early_b)
     for (int i = 0; i < min(nb, NS); ++i) issue_b(i);
+  // Inside lora_apply (the shrink wrote the Z operand) the first y copies
+  // start before the dependency wait: the shrink writes no y, and it lets
+  // this grid start only after its own dependency wait, by which time every
+  // earlier kernel on the stream (the last writer of y among them) has
+  // completed and its writes are visible.
+  const bool y_early = p.zt != nullptr;
+  if (y_early)
+    for (int i = 0; i < min(nb, NS); ++i) issue_y(i);
   griddep_wait();
   griddep_launch();
-  // Z written by the shrink as this tile's operand: one bulk copy per atom,
-  // ahead of the y copies
+  // Z written by the shrink as this tile's operand: one bulk copy per atom
   const uint32_t zt_bytes = (uint32_t)zt_entry_bytes(r, zf32);
   if (p.zt && tid == 0) {
     const uint8_t* src = p.zt + ((size_t)t * p.slices + sl) * zt_bytes;
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
   }
   for (int i = 0; i < min(nb, NS); ++i) {
     if (tid == 0 && !early_b) issue_b(i);
-    issue_y(i);
+    if (!y_early) issue_y(i);
   }
 
   // A operand: the tile's Z rows rounded to bf16 into the swizzled K-major
