@@ -12,8 +12,9 @@
 // host so that the grid fills the GPU about three blocks per SM; it does not
 // change any result). The A operand of the MMA, the tile's Z rows rounded to bf16,
 // is built once per block (coalesced loads, written by the threads straight
-// into the 128-byte-swizzled K-major layout) and serves all its column
-// blocks. Per column block: the B operand (64 rows of B_i x r) and the y tile
+// into the 128-byte-swizzled K-major layout), or, inside lora_apply, copied
+// in that layout from where the shrink wrote it (one bulk copy per 16 KB
+// atom), and serves all its column blocks. Per column block: the B operand (64 rows of B_i x r) and the y tile
 // (128 rows x 64 columns: one TMA box when the tile's tokens are
 // consecutive, else 16-byte asynchronous copies by every thread) come into
 // one of two stages, so the copies of

@@ -43,6 +43,12 @@
 // read the accumulator (warp w: token rows 32 (w % 4) .. + 31, one row per
 // thread, every other 32 columns from column 32 (w / 4)).
 //
+// Inside lora_apply (DET and UNSPLIT) the block that writes a final z value
+// also writes its bf16 parts into the expand's Z operand for the tile
+// (zt_entry_bytes layout), and zeroes the operand's rows past the tile's
+// tokens and ranks past r, so that the expand copies the operand instead of
+// building it; the rounding is the expand's own, so the bits are the same.
+//
 // Arithmetic order, fixed by K/S and r only: the tensor core's FP32
 // accumulation of the K-steps in order within the partition, then the
 // partitions summed in increasing order. A row's value depends only on that
