@@ -270,8 +270,12 @@ int lora_expand(const ig_shape* shape, const float* z, const void* B_stack,
  * shrink and expand run as one launch: the S partition blocks of a tile form
  * a thread-block cluster, sum their partials over distributed shared memory
  * in the same increasing partition order, and expand the tile's rows
- * (ig_plan_info.apply_kernels == 1; IG_FLAG_UNFUSED turns this off). The
- * results are bit-identical to the two-kernel sequence. */
+ * (ig_plan_info.apply_kernels == 1; IG_FLAG_UNFUSED turns this off). On
+ * the tcgen05 path (IG_PATH_MMA) in IG_MODE_DET and IG_MODE_UNSPLIT the
+ * shrink also writes the expand's bf16 Z operand into ws, the expand copies
+ * it instead of building it from z, and it starts its first y copies before
+ * its dependency wait (the shrink writes no y). The results are
+ * bit-identical to lora_shrink followed by lora_expand. */
 int lora_apply(const ig_shape* shape, const void* x, void* y,
                const int32_t* adapter_idx, const void* A_stack,
                const void* B_stack, float scale, float* z,
