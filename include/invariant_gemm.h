@@ -293,8 +293,10 @@ int lora_apply(const ig_shape* shape, const void* x, void* y,
  * a 4 MiB array inside the library, held by every GPU that loads it until
  * the process exits. This call allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.
- *   - Shapes whose ig_workspace_bytes exceeds 4 MiB are rejected with
- *     IG_ERR_WS_SMALL before anything is enqueued.
+ *   - Shapes whose shrink needs more than 4 MiB of workspace are rejected
+ *     with IG_ERR_WS_SMALL before anything is enqueued. That is
+ *     ig_workspace_bytes without the expand's Z operand, which only
+ *     lora_apply writes.
  *   - The first call on a device looks up the array's device address (with
  *     that device current). Make that first call before any stream capture.
  *   - Every call shares the one array and it keeps the previous call's

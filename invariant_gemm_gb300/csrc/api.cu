@@ -391,6 +391,40 @@ int run_expand(const ig_shape* sh, const Plan& pl, const float* z, const void* B
 }
 
 }  // namespace
+
+// Workspace bytes lora_shrink itself touches: everything before the expand's
+// Z operand, which only lora_apply writes. 0 for an invalid shape.
+size_t shrink_ws_bytes(const ig_shape* sh) {
+  Plan pl;
+  if (make_plan(sh, &pl) != IG_OK) return 0;
+  return pl.zt_bytes ? pl.off_zt : pl.total;
+}
+
+// lora_shrink with the workspace checked against shrink_ws_bytes when
+// `full` is false (the built-in scratch of lora_shrink_noalloc).
+int lora_shrink_ws(const ig_shape* shape, const void* x, const void* A_stack,
+                   const int32_t* adapter_idx, float scale, float* z, void* ws,
+                   size_t ws_bytes, void* stream, bool full) {
+  Plan pl;
+  int rc = make_plan(shape, &pl);
+  if (rc != IG_OK) return rc;
+  if (shape->M == 0) return IG_OK;
+  rc = check_ws(pl, ws, ws_bytes);
+  if (rc == IG_ERR_WS_SMALL && !full && ws_bytes >= shrink_ws_bytes(shape)) rc = IG_OK;
+  if (rc != IG_OK) return rc;
+  if (!x || !A_stack || !z) return IG_ERR_ARG;
+  if (!aligned16(x) || !aligned16(A_stack) || !aligned16(z) ||
+      (adapter_idx && !aligned16(adapter_idx)))
+    return IG_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (adapter_idx) {
+    rc = run_map(shape, pl, adapter_idx, w, st);
+    if (rc != IG_OK) return rc;
+  }
+  return run_shrink(shape, pl, x, A_stack, scale, z, w, st);
+}
+
 }  // namespace ig
 
 using namespace ig;
@@ -469,23 +503,7 @@ int ig_map_tokens(const ig_shape* shape, const int32_t* adapter_idx, void* ws, s
 int lora_shrink(const ig_shape* shape, const void* x, const void* A_stack,
                 const int32_t* adapter_idx, float scale, float* z, void* ws, size_t ws_bytes,
                 void* stream) {
-  Plan pl;
-  int rc = make_plan(shape, &pl);
-  if (rc != IG_OK) return rc;
-  if (shape->M == 0) return IG_OK;
-  rc = check_ws(pl, ws, ws_bytes);
-  if (rc != IG_OK) return rc;
-  if (!x || !A_stack || !z) return IG_ERR_ARG;
-  if (!aligned16(x) || !aligned16(A_stack) || !aligned16(z) ||
-      (adapter_idx && !aligned16(adapter_idx)))
-    return IG_ERR_ALIGN;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  if (adapter_idx) {
-    rc = run_map(shape, pl, adapter_idx, w, st);
-    if (rc != IG_OK) return rc;
-  }
-  return run_shrink(shape, pl, x, A_stack, scale, z, w, st);
+  return lora_shrink_ws(shape, x, A_stack, adapter_idx, scale, z, ws, ws_bytes, stream, true);
 }
 
 int lora_expand(const ig_shape* shape, const float* z, const void* B_stack,

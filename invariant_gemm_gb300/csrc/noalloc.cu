@@ -16,6 +16,15 @@
 #include "ig_common.cuh"
 
 namespace ig {
+
+// api.cu: lora_shrink's own share of the workspace (the expand's Z operand,
+// which only lora_apply writes, left out), and lora_shrink checking the
+// workspace against it
+size_t shrink_ws_bytes(const ig_shape* sh);
+int lora_shrink_ws(const ig_shape* shape, const void* x, const void* A_stack,
+                   const int32_t* adapter_idx, float scale, float* z, void* ws,
+                   size_t ws_bytes, void* stream, bool full);
+
 namespace {
 
 // 4 MiB: the fixed counter area plus room for decode-sized token maps and
@@ -64,7 +73,7 @@ extern "C" int lora_shrink_noalloc(const ig_shape* shape, const void* x, const v
   auto aligned16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
   if (!aligned16(x) || !aligned16(A_stack) || !aligned16(z) || !aligned16(adapter_idx))
     return IG_ERR_ALIGN;
-  if ((size_t)info.workspace_bytes > kNoAllocScratchBytes) return IG_ERR_WS_SMALL;
+  if (shrink_ws_bytes(shape) > kNoAllocScratchBytes) return IG_ERR_WS_SMALL;
   void* ws = nullptr;
   rc = scratch_for_current_device(&ws);
   if (rc != IG_OK) return rc;
@@ -74,5 +83,6 @@ extern "C" int lora_shrink_noalloc(const ig_shape* shape, const void* x, const v
   const size_t clear = kCountersOffset + 4 * (size_t)slots;
   if (cudaMemsetAsync(ws, 0, clear, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return IG_ERR_CUDA;
-  return lora_shrink(shape, x, A_stack, adapter_idx, scale, z, ws, kNoAllocScratchBytes, stream);
+  return lora_shrink_ws(shape, x, A_stack, adapter_idx, scale, z, ws, kNoAllocScratchBytes,
+                        stream, false);
 }

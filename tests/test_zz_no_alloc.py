@@ -111,3 +111,20 @@ def test_noalloc_rejects_bad_pointers_before_enqueueing():
     # and the next valid call is still right
     z2 = _noalloc(p, sh)
     _same_bits(z2, _existing(p, sh))
+
+
+def test_noalloc_needs_only_the_shrinks_share():
+    """ig_workspace_bytes also counts the expand's Z operand that lora_apply
+    writes on the tcgen05 path (three bf16 parts per value with FP32 Z); the
+    shrink alone never touches it, so a shape whose full workspace is past
+    4 MiB but whose shrink share fits still runs here."""
+    need_gpu()
+    p = synth.make_problem(2048, 1024, 512, 64, slices=3, L=16, seed=1261, none_frac=0.05,
+                           device="cuda")
+    sh = ig.make_shape(p.M, p.K, p.N, p.r, slices=3, num_adapters=16, split_k=8,
+                       mode=ig.MODE_UNSPLIT, flags=ig.FLAG_Z_FP32)
+    assert ig.plan_query(sh)["path"] == ig.PATH_MMA
+    assert ig.workspace_bytes(sh) > (4 << 20)
+    z = _noalloc(p, sh)
+    _same_bits(z, _existing(p, sh))
+    check_shrink(p, z)
