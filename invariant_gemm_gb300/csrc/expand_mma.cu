@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(128 * WG, WG == 1 ? 3 : 2)
 
   // A operand: the tile's Z rows rounded to bf16 into the swizzled K-major
   // layout (16-byte chunk c of a 128-byte row m sits at chunk c ^ (m % 8)),
-  // rows past nrows zero. Warp w loads rows 32w .. 32w+31, r/4 lanes per row
+  // rows past nrows zero. Each warp loads its 128 / warps rows, r/4 lanes per row
   // (4 values each, coalesced), 16 loads in flight per lane before any is
   // used (one at a time, each load's latency under the copies in flight
   // added up to most of the block's life). With FP32 Z also
