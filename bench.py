@@ -808,6 +808,8 @@ PROFILE_CASES = {
     # name: (M, K, N, r, slices, L, adapter ids, Split-K, entry point)
     "qkv-shrink": (4096, 4096, 4096, 64, 3, 16, "segments", 8, "shrink"),
     "qkv-expand": (4096, 4096, 4096, 64, 3, 16, "segments", 8, "expand"),
+    "down-shrink": (4096, 11008, 4096, 64, 1, 16, "segments", 8, "shrink"),
+    "down-expand": (4096, 11008, 4096, 64, 1, 16, "segments", 8, "expand"),
     "scattered-shrink": (8192, 8192, 8192, 128, 1, 64, "zipf", 4, "shrink"),
     "scattered-expand": (8192, 8192, 8192, 128, 1, 64, "zipf", 4, "expand"),
 }
