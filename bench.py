@@ -883,6 +883,88 @@ def reference_main(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# size-dependent copy ceiling (context for the roofline fractions)
+# ---------------------------------------------------------------------------
+
+def ceiling_main():
+    print(json.dumps(ceiling_points(torch.device("cuda", 0))))
+    return 0
+
+
+def ceiling_points(device):
+    """What a plain elementwise device kernel (torch `neg`: one read, one
+    write per element) reaches when it moves as many bytes as one call of
+    each timed workload, half read and half written, timed like that
+    workload: one call per CUDA-graph replay with L2 flushed before it (the
+    prefill points), and 64 calls of the decode layer's size on distinct
+    buffers back to back in one graph (the decode layers). Writes still in L2
+    when a call ends count as moved, as they do for the library's kernels.
+    Calibration: a 4 GB copy (torch `copy_`, as the measured peak was taken)
+    and a 4 GB `neg`, outside graphs, best of 10."""
+    timer = CallTimer(device)
+    peak, kind = measured_peaks()
+    qkv = alg_bytes(4096, 4096, 4096, 64, 3, 16)
+    down = alg_bytes(4096, 11008, 4096, 64, 1, 16)
+    dec = alg_bytes(256, 4096, 4096, 16, 1, 8)["total"]
+    sizes = (("decode_layer", dec), ("qkv_shrink", qkv["shrink"]),
+             ("qkv_expand", qkv["expand"]), ("qkv_apply", qkv["total"]),
+             ("down_apply", down["total"]), ("neg_1GB", 1 << 30))
+    out = {"what": " ".join(ceiling_points.__doc__.split()), "peak": peak, "peak_kind": kind,
+           "points": {}}
+
+    def point(nbytes, us):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"bytes": int(nbytes), "us": us, "gbs": gbs, "frac_of_peak": gbs / peak}
+
+    for name, nbytes in sizes:
+        n = nbytes // 4   # bf16 elements of each buffer: nbytes / 2 read, nbytes / 2 written
+        a = torch.ones(n, dtype=torch.bfloat16, device=device)
+        b = torch.empty_like(a)
+
+        def body(stream, a=a, b=b):
+            with torch.cuda.stream(stream):
+                torch.neg(a, out=b)
+        out["points"][name] = point(4 * n, timer.time(body, 9))
+        del a, b
+        torch.cuda.empty_cache()
+    n = dec // 4
+    bufs = [(torch.ones(n, dtype=torch.bfloat16, device=device),
+             torch.empty(n, dtype=torch.bfloat16, device=device)) for _ in range(64)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for a, b in bufs:
+            torch.neg(a, out=b)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for a, b in bufs:
+            torch.neg(a, out=b)
+    ms = time_graph(g, 20, 5, 1, device)
+    out["points"]["decode_layer_x64_one_graph"] = point(4 * n, ms * 1e3 / 64)
+    del bufs, g
+    torch.cuda.empty_cache()
+    n = 1 << 30
+    a = torch.ones(n, dtype=torch.bfloat16, device=device)
+    b = torch.empty_like(a)
+    for name, fn in (("copy_4GB_no_graph", lambda: b.copy_(a)),
+                     ("neg_4GB_no_graph", lambda: torch.neg(a, out=b))):
+        best = None
+        for _ in range(11):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) * 1e3
+            best = t if best is None else min(best, t)
+        out["points"][name] = point(4 * n, best)
+    del a, b
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
 
@@ -901,10 +983,14 @@ def main():
                     help="identical-input replays per variant for the mismatch statistics")
     ap.add_argument("--profile-case", choices=["decode"] + sorted(PROFILE_CASES),
                     help="run a few calls of one kernel on a fixed workload (for ncu) and exit")
+    ap.add_argument("--ceiling", action="store_true",
+                    help="time a plain device copy of each workload's byte count and exit")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.profile_case:
         return profile_case(args.profile_case)
+    if args.ceiling:
+        return ceiling_main()
 
     if args.impl == "reference":
         return reference_main(args, rank, world)
@@ -1158,6 +1244,15 @@ def main():
            "e2e": e2e,
            "hbm_gbs": det["hbm_gbs"]}
     if rank == 0:
+        # context for the fractions: a plain elementwise kernel moving the same
+        # bytes, timed the same way (single GPU work, after every timed region)
+        ceil = ceiling_points(device)
+        dl = ceil["points"]["decode_layer_x64_one_graph"]
+        roofline["same_bytes_elementwise_kernel"] = {
+            "us_per_launch": dl["us"], "frac": dl["frac_of_peak"],
+            "how": "torch neg moving 8,423,424 bytes (half read, half written), 64 launches "
+                   "on distinct buffers back to back in one CUDA graph"}
+        out["same_bytes_ceiling"] = ceil
         out["cpu_baseline"] = cpu_baseline_obj(args.cpu_seconds, args.cpu_config_seconds)
         print(json.dumps(out))
     if world > 1:
